@@ -1,0 +1,158 @@
+/*
+ * nvfp4_gemv.h -- C ABI of the GB300 (sm_103a) NVFP4 batched decode GEMV.
+ *
+ * The operation (atlas pull request #266, "perf(decode): n>=4 tiled QKV +
+ * o_proj GEMV for NVFP4 batched decode", section "What it does"): for a tile
+ * of n concurrent decode tokens, compute the attention projection
+ *
+ *     Y[t, r] = bf16( g * sum_{k<K} X[t, k] * E2M1(W[r, k]) * E4M3(S[r, k/16]) )
+ *
+ * for t < n, r < N, reading the NVFP4 weight matrix from HBM once for all n
+ * tokens instead of once per token.  The same pull request's section
+ * "Correctness argument" and its review thread's "Numeric identity" caveat fix
+ * the invariant this library keeps: a batched call returns, bit for bit, what
+ * n single-token (n == 1) calls of the same variant return.
+ *
+ * Data layout (all row-major, no padding, no swizzle):
+ *   w_packed       [N][K/2] bytes   E2M1 codes; element 2i of a row is the LOW
+ *                                    nibble of byte i, element 2i+1 the high one.
+ *   w_scale_e4m3   [N][K/16] bytes  one E4M3 scale per 16 consecutive k.
+ *   w_global_scale 1 float          fp32 global scale g.
+ *   x_bf16         [n][K] bf16      activations (uint16 bit patterns).
+ *   y_bf16         [n][N] bf16      output, fully overwritten.
+ * E2M1: 1 sign, 2 exponent, 1 mantissa bit (OCP Microscaling Formats v1.0).
+ * E4M3: bias 7, max 448, S.1111.111 = NaN (OCP 8-bit floating point).
+ *
+ * Conventions shared by every entry point:
+ *   - The caller owns every buffer; the library never frees or keeps them.
+ *   - Device calls are asynchronous on `stream` and never synchronize it.
+ *   - y_bf16 must not overlap any input.
+ *   - On a non-OK status nothing was launched, and nvfp4_last_error() returns
+ *     a message for this thread.
+ *   - Pointers named "device" must be device (or managed) memory of the
+ *     current device; pointers named "host" must be host memory.
+ */
+#ifndef NVFP4_GEMV_H
+#define NVFP4_GEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nvfp4_status {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1,     /* null pointer, bad size, K % 16 != 0, ... */
+    NVFP4_ERR_MISALIGNED = 2,      /* reserved: unaligned inputs take a slower kernel instead */
+    NVFP4_ERR_UNSUPPORTED = 3,     /* device is not sm_103, or option not available */
+    NVFP4_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed; see nvfp4_last_error() */
+    NVFP4_ERR_DEVICE_TIMEOUT = 5,  /* a kernel gave up waiting on a barrier (see nvfp4_device_error) */
+    NVFP4_ERR_WORKSPACE = 6        /* caller workspace too small */
+} nvfp4_status;
+
+/* Kernel variants (selectable through nvfp4_gemv_opts; AUTO picks per shape). */
+typedef enum nvfp4_variant {
+    NVFP4_VARIANT_AUTO = 0,
+    NVFP4_VARIANT_MMA = 1,      /* TMA ring + register dequant + mma.sync f16 tensor cores */
+    NVFP4_VARIANT_SIMT = 2,     /* TMA ring + register dequant + fp32 CUDA-core FMAs */
+    NVFP4_VARIANT_GENERIC = 3   /* plain loads, any K % 16 == 0 and any alignment */
+} nvfp4_variant;
+
+/* Token tiling.  ONE_PASS streams W once for all n tokens (chunks of up to 16
+ * tokens when n > 16 or shared memory is short).  GREEDY_321 is the pages'
+ * prior art (atlas #266, "What it does"): tiles of 3 tokens, then a 2 or 1
+ * remainder, each tile re-reading W -- kept to measure against. */
+typedef enum nvfp4_tiling {
+    NVFP4_TILING_AUTO = 0,
+    NVFP4_TILING_ONE_PASS = 1,
+    NVFP4_TILING_GREEDY_321 = 2
+} nvfp4_tiling;
+
+typedef struct nvfp4_gemv_opts {
+    int variant;             /* nvfp4_variant */
+    int tiling;              /* nvfp4_tiling */
+    int num_ctas;            /* 0 = one CTA per SM; else 1..#SMs (persistent grid size) */
+    int stages;              /* 0 = as many TMA ring stages as shared memory allows; else 2..8 */
+    void *workspace;         /* NULL = library-owned per-stream workspace; else device memory */
+    size_t workspace_bytes;  /* size of `workspace` (see nvfp4_gemv_workspace_size) */
+} nvfp4_gemv_opts;
+
+/* Launch plan the library would use (for tests and benchmarks). */
+typedef struct nvfp4_gemv_plan_info {
+    int variant;         /* resolved nvfp4_variant */
+    int tiling;          /* resolved nvfp4_tiling */
+    int passes;          /* weight passes (token tiles) */
+    int tile_tokens[16]; /* tokens per pass (first 16 passes) */
+    int num_ctas;        /* grid size of each launch */
+    int stages;          /* TMA ring stages */
+    int smem_bytes;      /* dynamic shared memory per CTA */
+    long long units;     /* work units (128 rows x 128 k) per pass */
+} nvfp4_gemv_plan_info;
+
+/*
+ * Y[n][N] = X[n][K] . W^T with NVFP4 W (see the file header for the formula).
+ *
+ * w_packed, w_scale_e4m3, w_global_scale_f32, x_bf16: device, read only.
+ * y_bf16: device, written.  n >= 0 (n == 0 is a no-op), N >= 1, K >= 16 and
+ * K % 16 == 0.  Any n is accepted; more than 16 tokens (or fewer when
+ * n * K is too large for shared memory) are processed in chunks that each
+ * re-read W.  The fast path needs K % 256 == 0 and 16-byte aligned w_packed,
+ * w_scale_e4m3 and x_bf16; other inputs take the GENERIC kernel.
+ * Uses a library-owned workspace tied to `stream`, allocated on the first call
+ * on that stream (make that first call before capturing `stream` in a graph).
+ * Calls on different streams may run concurrently.
+ * Returns NVFP4_OK or an error status; never synchronizes.
+ */
+nvfp4_status nvfp4_gemv_batched(const uint8_t *w_packed, const uint8_t *w_scale_e4m3,
+                                const float *w_global_scale_f32, const uint16_t *x_bf16,
+                                uint16_t *y_bf16, int n, int N, int K, cudaStream_t stream);
+
+/* Same as nvfp4_gemv_batched with explicit options (NULL = defaults).  With a
+ * caller workspace, concurrent calls must use distinct workspaces; the first
+ * use of a workspace must see it zeroed (cudaMemset), and every completed call
+ * leaves it zeroed again. */
+nvfp4_status nvfp4_gemv_batched_ex(const uint8_t *w_packed, const uint8_t *w_scale_e4m3,
+                                   const float *w_global_scale_f32, const uint16_t *x_bf16,
+                                   uint16_t *y_bf16, int n, int N, int K, cudaStream_t stream,
+                                   const nvfp4_gemv_opts *opts);
+
+/* Bytes of device workspace a call with these options needs (opts may be NULL). */
+nvfp4_status nvfp4_gemv_workspace_size(int n, int N, int K, const nvfp4_gemv_opts *opts,
+                                       size_t *bytes);
+
+/* Describe the launches nvfp4_gemv_batched_ex would make, without launching.
+ * Pointer alignment is taken as 16 bytes (the fast path's requirement). */
+nvfp4_status nvfp4_gemv_plan(int n, int N, int K, const nvfp4_gemv_opts *opts,
+                             nvfp4_gemv_plan_info *info);
+
+/*
+ * Host-side NVFP4 quantizer for making test data (not on the GEMV path).
+ * w: host fp32 [N][K]; w_packed: host [N][K/2]; w_scale: host [N][K/16];
+ * global_scale: host, 1 float.  amax = max|w|; g = amax / (6 * 448) in fp32
+ * (1 when amax == 0); s = E4M3_rne_sat(blockabsmax / (6 g)); code =
+ * E2M1_rne_sat(w / (E4M3(s) g)), code 0 when the magnitude rounds to 0 or s is
+ * 0.  All arithmetic fp32.  Non-finite input -> NVFP4_ERR_INVALID_ARG.
+ */
+nvfp4_status nvfp4_quantize_ref(const float *w, int N, int K, uint8_t *w_packed, uint8_t *w_scale,
+                                float *global_scale);
+
+/* Synchronize `stream`, then report and clear the library's device error word.
+ * *code receives the raw word (0 = no error).  Returns NVFP4_ERR_DEVICE_TIMEOUT
+ * when a kernel gave up on a wait; the library then also re-zeroes its own
+ * workspaces so later calls start clean. */
+nvfp4_status nvfp4_device_error(cudaStream_t stream, int *code);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char *nvfp4_last_error(void);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int nvfp4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GEMV_H */

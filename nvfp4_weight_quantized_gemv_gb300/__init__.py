@@ -1,0 +1,204 @@
+"""GB300 (sm_103a) NVFP4 batched decode GEMV -- Python binding of the C ABI.
+
+Thin ctypes marshalling over ``libnvfp4_gemv.so`` (declared in
+``include/nvfp4_gemv.h``).  Functions carry the C entry points' names and
+take torch tensors (device memory, streams) or numpy arrays (host quantizer);
+every step of the computation runs in the library's CUDA kernels.  If the
+library is missing the import of any entry point raises -- there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libnvfp4_gemv.so")
+
+# nvfp4_status
+NVFP4_OK = 0
+NVFP4_ERR_INVALID_ARG = 1
+NVFP4_ERR_MISALIGNED = 2
+NVFP4_ERR_UNSUPPORTED = 3
+NVFP4_ERR_CUDA = 4
+NVFP4_ERR_DEVICE_TIMEOUT = 5
+NVFP4_ERR_WORKSPACE = 6
+
+# nvfp4_variant / nvfp4_tiling
+VARIANT_AUTO, VARIANT_MMA, VARIANT_SIMT, VARIANT_GENERIC = 0, 1, 2, 3
+TILING_AUTO, TILING_ONE_PASS, TILING_GREEDY_321 = 0, 1, 2
+VARIANT_NAMES = {0: "auto", 1: "mma", 2: "simt", 3: "generic"}
+TILING_NAMES = {0: "auto", 1: "one_pass", 2: "greedy_321"}
+
+# Names the C ABI exports (include/nvfp4_gemv.h).
+EXPORTS = ("nvfp4_gemv_batched", "nvfp4_gemv_batched_ex", "nvfp4_gemv_workspace_size", "nvfp4_gemv_plan",
+           "nvfp4_quantize_ref", "nvfp4_device_error", "nvfp4_last_error", "nvfp4_version")
+
+
+class Nvfp4Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"nvfp4 status {status}: {message}")
+        self.status = status
+
+
+class nvfp4_gemv_opts(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("tiling", ctypes.c_int), ("num_ctas", ctypes.c_int),
+                ("stages", ctypes.c_int), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+class nvfp4_gemv_plan_info(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("tiling", ctypes.c_int), ("passes", ctypes.c_int),
+                ("tile_tokens", ctypes.c_int * 16), ("num_ctas", ctypes.c_int), ("stages", ctypes.c_int),
+                ("smem_bytes", ctypes.c_int), ("units", ctypes.c_longlong)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """Load the shared library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -m nvfp4_weight_quantized_gemv_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            L.nvfp4_gemv_batched.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
+            L.nvfp4_gemv_batched.restype = i
+            L.nvfp4_gemv_batched_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp, ctypes.POINTER(nvfp4_gemv_opts)]
+            L.nvfp4_gemv_batched_ex.restype = i
+            L.nvfp4_gemv_workspace_size.argtypes = [i, i, i, ctypes.POINTER(nvfp4_gemv_opts), ctypes.POINTER(sz)]
+            L.nvfp4_gemv_workspace_size.restype = i
+            L.nvfp4_gemv_plan.argtypes = [i, i, i, ctypes.POINTER(nvfp4_gemv_opts),
+                                          ctypes.POINTER(nvfp4_gemv_plan_info)]
+            L.nvfp4_gemv_plan.restype = i
+            L.nvfp4_quantize_ref.argtypes = [vp, i, i, vp, vp, vp]
+            L.nvfp4_quantize_ref.restype = i
+            L.nvfp4_device_error.argtypes = [vp, ctypes.POINTER(i)]
+            L.nvfp4_device_error.restype = i
+            L.nvfp4_last_error.argtypes = []
+            L.nvfp4_last_error.restype = ctypes.c_char_p
+            L.nvfp4_version.argtypes = []
+            L.nvfp4_version.restype = i
+            _lib = L
+    return _lib
+
+
+def nvfp4_last_error() -> str:
+    return lib().nvfp4_last_error().decode()
+
+
+def nvfp4_version() -> int:
+    return lib().nvfp4_version()
+
+
+def _check(status: int):
+    if status != NVFP4_OK:
+        raise Nvfp4Error(status, nvfp4_last_error())
+
+
+def _opts(variant=0, tiling=0, num_ctas=0, stages=0, workspace=None):
+    o = nvfp4_gemv_opts()
+    o.variant, o.tiling, o.num_ctas, o.stages = int(variant), int(tiling), int(num_ctas), int(stages)
+    if workspace is not None:
+        o.workspace = workspace.data_ptr()
+        o.workspace_bytes = workspace.numel() * workspace.element_size()
+    return o
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _gemv_args(w_packed, w_scale, w_global_scale, x, y):
+    import torch
+    for name, t, dt in (("w_packed", w_packed, torch.uint8), ("w_scale", w_scale, torch.uint8),
+                        ("w_global_scale", w_global_scale, torch.float32), ("y", y, torch.bfloat16)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous CUDA {dt} tensor")
+    if x.dtype not in (torch.bfloat16,) or not x.is_cuda or not x.is_contiguous():
+        raise TypeError("x must be a contiguous CUDA bfloat16 tensor")
+    N = w_packed.shape[0]
+    K = 2 * w_packed.shape[1]
+    n = x.shape[0] if x.dim() == 2 else 1
+    if w_scale.shape != (N, K // 16) or x.numel() != n * K or y.numel() != n * N:
+        raise ValueError("shape mismatch: w_packed [N, K/2], w_scale [N, K/16], x [n, K], y [n, N]")
+    return n, N, K
+
+
+def nvfp4_gemv_batched(w_packed, w_scale, w_global_scale, x, y=None, stream=None):
+    """Y[n, N] = X[n, K] . W^T (see include/nvfp4_gemv.h).  Returns y."""
+    import torch
+    if y is None:
+        n = x.shape[0] if x.dim() == 2 else 1
+        y = torch.empty((n, w_packed.shape[0]), dtype=torch.bfloat16, device=x.device)
+    n, N, K = _gemv_args(w_packed, w_scale, w_global_scale, x, y)
+    _check(lib().nvfp4_gemv_batched(w_packed.data_ptr(), w_scale.data_ptr(), w_global_scale.data_ptr(),
+                                    x.data_ptr(), y.data_ptr(), n, N, K, _stream_handle(stream)))
+    return y
+
+
+def nvfp4_gemv_batched_ex(w_packed, w_scale, w_global_scale, x, y=None, stream=None, variant=0, tiling=0,
+                          num_ctas=0, stages=0, workspace=None):
+    """nvfp4_gemv_batched with explicit variant / tiling / grid / ring depth / workspace."""
+    import torch
+    if y is None:
+        n = x.shape[0] if x.dim() == 2 else 1
+        y = torch.empty((n, w_packed.shape[0]), dtype=torch.bfloat16, device=x.device)
+    n, N, K = _gemv_args(w_packed, w_scale, w_global_scale, x, y)
+    o = _opts(variant, tiling, num_ctas, stages, workspace)
+    _check(lib().nvfp4_gemv_batched_ex(w_packed.data_ptr(), w_scale.data_ptr(), w_global_scale.data_ptr(),
+                                       x.data_ptr(), y.data_ptr(), n, N, K, _stream_handle(stream),
+                                       ctypes.byref(o)))
+    return y
+
+
+def nvfp4_gemv_workspace_size(n, N, K, variant=0, tiling=0, num_ctas=0, stages=0) -> int:
+    b = ctypes.c_size_t(0)
+    o = _opts(variant, tiling, num_ctas, stages)
+    _check(lib().nvfp4_gemv_workspace_size(n, N, K, ctypes.byref(o), ctypes.byref(b)))
+    return b.value
+
+
+def nvfp4_gemv_plan(n, N, K, variant=0, tiling=0, num_ctas=0, stages=0) -> dict:
+    info = nvfp4_gemv_plan_info()
+    o = _opts(variant, tiling, num_ctas, stages)
+    _check(lib().nvfp4_gemv_plan(n, N, K, ctypes.byref(o), ctypes.byref(info)))
+    return dict(variant=VARIANT_NAMES[info.variant], tiling=TILING_NAMES[info.tiling], passes=info.passes,
+                tile_tokens=list(info.tile_tokens[:min(info.passes, 16)]), num_ctas=info.num_ctas,
+                stages=info.stages, smem_bytes=info.smem_bytes, units=info.units)
+
+
+def nvfp4_quantize_ref(w):
+    """Host quantizer: fp32 numpy W[N, K] -> (packed uint8 [N, K/2], scale uint8 [N, K/16], g float)."""
+    import numpy as np
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    N, K = w.shape
+    packed = np.empty((N, K // 2), dtype=np.uint8)
+    scale = np.empty((N, K // 16), dtype=np.uint8)
+    g = np.zeros(1, dtype=np.float32)
+    _check(lib().nvfp4_quantize_ref(w.ctypes.data, N, K, packed.ctypes.data, scale.ctypes.data, g.ctypes.data))
+    return packed, scale, float(g[0])
+
+
+def nvfp4_device_error(stream=None) -> int:
+    """Synchronize, read and clear the device error word; raises Nvfp4Error on a device timeout."""
+    code = ctypes.c_int(0)
+    st = lib().nvfp4_device_error(_stream_handle(stream), ctypes.byref(code))
+    if st != NVFP4_OK and st != NVFP4_ERR_DEVICE_TIMEOUT:
+        _check(st)
+    if st == NVFP4_ERR_DEVICE_TIMEOUT:
+        raise Nvfp4Error(st, nvfp4_last_error())
+    return code.value
+
+
+def build(force: bool = False) -> str:
+    from .build import build as _build
+    return _build(force=force)

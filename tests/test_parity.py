@@ -1,0 +1,247 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Tolerance on bf16 outputs: |y_gpu - y_ref| <= 1e-2 * (|y_ref| + 1), with y_ref
+the oracle's unrounded fp64 value.  Within one variant a batched call equals
+the n single-token calls bit for bit (atlas #266, "Correctness argument").
+Inputs: oracle-quantized W ~ N(0, 0.02), X ~ N(0, 1) bf16 (synth.py).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_weight_quantized_gemv_gb300 as nv
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+VARIANTS = {"mma": nv.VARIANT_MMA, "simt": nv.VARIANT_SIMT, "generic": nv.VARIANT_GENERIC}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    nv.build()
+    oracle.build()
+
+
+def make_case(N, K, n, wseed=0, xseed=1, outlier=0.0):
+    w = synth.weights_f32(N, K, wseed)
+    packed, scale, g = oracle.quantize(w)
+    x = synth.activations_bf16(n, K, xseed, outlier)
+    return packed, scale, g, x
+
+
+def to_gpu(packed, scale, g, x):
+    wp = torch.from_numpy(np.ascontiguousarray(packed)).cuda()
+    ws = torch.from_numpy(np.ascontiguousarray(scale)).cuda()
+    gs = torch.tensor([g], dtype=torch.float32, device="cuda")
+    xt = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda().view(torch.bfloat16)
+    return wp, ws, gs, xt
+
+
+def gpu_gemv(dev, variant=0, tiling=0, **kw):
+    wp, ws, gs, xt = dev
+    y = nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt, variant=variant, tiling=tiling, **kw)
+    torch.cuda.synchronize()
+    return y.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def bf16_to_f64(y16):
+    return torch.from_numpy(np.ascontiguousarray(y16).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def assert_close(y16, y64):
+    yv = bf16_to_f64(y16)
+    err = np.abs(yv - y64)
+    bound = TOL * (np.abs(y64) + 1.0)
+    bad = ~(err <= bound)
+    assert not bad.any(), f"{bad.sum()} outputs out of tolerance; worst err {err.max()} at {np.argmax(err)}"
+
+
+# ------------------------------------------------------------ small, full
+@pytest.mark.parametrize("variant", list(VARIANTS))
+@pytest.mark.parametrize("tiling", [nv.TILING_ONE_PASS, nv.TILING_GREEDY_321])
+def test_tiny_workload_full_output(variant, tiling):
+    # N=256, K=512, n=3 tokens, W seed 0, X seed 0
+    packed, scale, g, x = make_case(256, 512, 3, 0, 0)
+    y64, _ = oracle.gemv(packed, scale, g, x)
+    y16 = gpu_gemv(to_gpu(packed, scale, g, x), VARIANTS[variant], tiling)
+    assert_close(y16, y64)
+
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
+@pytest.mark.parametrize("N,K,n", [(1000, 1024, 5), (200, 512, 16), (129, 256, 9), (1, 256, 1), (384, 2048, 8)])
+def test_ragged_shapes_full_output(variant, N, K, n):
+    packed, scale, g, x = make_case(N, K, n, 3, 4, outlier=0.01)
+    y64, _ = oracle.gemv(packed, scale, g, x)
+    y16 = gpu_gemv(to_gpu(packed, scale, g, x), VARIANTS[variant])
+    assert_close(y16, y64)
+
+
+def test_one_hot_pins_nibble_order_and_scale_placement():
+    """Single-term outputs are exact: y[t, r] = bf16(E2M1 * E4M3 * g) at k_t."""
+    N, K = 128, 256
+    packed, scale, g, _ = make_case(N, K, 1, 9, 0)
+    for variant in ("mma", "simt"):
+        for k0 in range(0, K, 16):
+            x = np.zeros((16, K), dtype=np.uint16)
+            x[np.arange(16), k0 + np.arange(16)] = 0x3F80
+            _, want = oracle.gemv(packed, scale, g, x)
+            got = gpu_gemv(to_gpu(packed, scale, g, x), VARIANTS[variant])
+            assert np.array_equal(got, want), (variant, k0)
+
+
+# ----------------------------------------------------------- invariants
+@pytest.mark.parametrize("variant", list(VARIANTS))
+def test_batched_equals_single_token_calls(variant):
+    N, K, n = 1536, 2048, 16
+    packed, scale, g, x = make_case(N, K, n, 5, 6)
+    full = gpu_gemv(to_gpu(packed, scale, g, x), VARIANTS[variant])
+    for t in range(n):
+        one = gpu_gemv(to_gpu(packed, scale, g, x[t:t + 1]), VARIANTS[variant])
+        assert np.array_equal(one[0], full[t]), t
+    greedy = gpu_gemv(to_gpu(packed, scale, g, x), VARIANTS[variant], nv.TILING_GREEDY_321)
+    assert np.array_equal(greedy, full)
+
+
+def test_repeat_calls_are_bit_identical():
+    packed, scale, g, x = make_case(2048, 1536, 7, 1, 2)
+    dev = to_gpu(packed, scale, g, x)
+    first = gpu_gemv(dev)
+    for _ in range(3):
+        assert np.array_equal(gpu_gemv(dev), first)
+
+
+@pytest.mark.parametrize("num_ctas,stages", [(1, 2), (3, 0), (7, 3), (0, 2), (150, 8)])
+def test_grid_and_ring_options(num_ctas, stages):
+    packed, scale, g, x = make_case(700, 1280, 4, 7, 8)
+    y64, _ = oracle.gemv(packed, scale, g, x)
+    y16 = gpu_gemv(to_gpu(packed, scale, g, x), nv.VARIANT_MMA, num_ctas=num_ctas, stages=stages)
+    assert_close(y16, y64)
+
+
+def test_generic_paths_for_unaligned_or_ragged_k():
+    # K % 256 != 0 -> generic kernel
+    packed, scale, g, x = make_case(300, 784, 3, 2, 3)
+    y64, _ = oracle.gemv(packed, scale, g, x)
+    assert_close(gpu_gemv(to_gpu(packed, scale, g, x)), y64)
+    # misaligned activation pointer -> generic kernel, same answer
+    packed, scale, g, x = make_case(256, 512, 2, 2, 3)
+    wp, ws, gs, _ = to_gpu(packed, scale, g, x)
+    buf = torch.zeros(2 * 512 + 8, dtype=torch.int16, device="cuda")
+    buf[1:1 + 2 * 512] = torch.from_numpy(x.view(np.int16).ravel()).cuda()
+    xt = buf[1:1 + 2 * 512].view(torch.bfloat16).view(2, 512)
+    y = nv.nvfp4_gemv_batched(wp, ws, gs, xt)
+    torch.cuda.synchronize()
+    y64, _ = oracle.gemv(packed, scale, g, x)
+    assert_close(y.view(torch.int16).cpu().numpy().view(np.uint16), y64)
+
+
+def test_more_than_16_tokens_and_noop():
+    packed, scale, g, x = make_case(512, 1024, 21, 4, 5)
+    y64, _ = oracle.gemv(packed, scale, g, x)
+    dev = to_gpu(packed, scale, g, x)
+    assert_close(gpu_gemv(dev), y64)
+    wp, ws, gs, xt = dev
+    y = torch.full((0, 512), 7.0, dtype=torch.bfloat16, device="cuda")
+    nv.nvfp4_gemv_batched(wp, ws, gs, xt[:0].contiguous(), y)
+
+
+def test_output_guard_bands_untouched():
+    N, K, n = 333, 512, 5
+    packed, scale, g, x = make_case(N, K, n, 6, 7)
+    wp, ws, gs, xt = to_gpu(packed, scale, g, x)
+    pad = 64
+    buf = torch.full((n * N + 2 * pad,), 12345, dtype=torch.int16, device="cuda")
+    y = buf[pad:pad + n * N].view(torch.bfloat16).view(n, N)
+    for variant in VARIANTS.values():
+        nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt, y, variant=variant)
+        torch.cuda.synchronize()
+        b = buf.cpu().numpy()
+        assert np.all(b[:pad] == 12345) and np.all(b[pad + n * N:] == 12345)
+
+
+def test_caller_workspace():
+    packed, scale, g, x = make_case(1024, 2048, 3, 8, 9)
+    wp, ws, gs, xt = to_gpu(packed, scale, g, x)
+    nbytes = nv.nvfp4_gemv_workspace_size(3, 1024, 2048)
+    work = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    y = nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt, workspace=work)
+    y2 = nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt, workspace=work)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+    y64, _ = oracle.gemv(packed, scale, g, x)
+    assert_close(y.view(torch.int16).cpu().numpy().view(np.uint16), y64)
+    small = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(nv.Nvfp4Error):
+        nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt, workspace=small)
+
+
+def test_activation_beyond_f16_range_is_rescaled():
+    packed, scale, g, x = make_case(256, 1024, 4, 1, 1)
+    xf = synth.activations_f32(4, 1024, 1)
+    xf[1, 17] = 3.0e5            # beyond f16's range
+    xf[2, 900] = -1.0e6
+    x = synth.to_bf16_bits(xf)
+    y64, _ = oracle.gemv(packed, scale, g, x)
+    for variant in ("mma", "simt", "generic"):
+        assert_close(gpu_gemv(to_gpu(packed, scale, g, x), VARIANTS[variant]), y64)
+
+
+def test_nan_scale_propagates():
+    packed, scale, g, x = make_case(256, 512, 2, 1, 1)
+    scale = scale.copy()
+    scale[10, 3] = 0x7F
+    y64, _ = oracle.gemv(packed, scale, g, x)
+    for variant in VARIANTS.values():
+        y16 = gpu_gemv(to_gpu(packed, scale, g, x), variant)
+        yv = bf16_to_f64(y16)
+        assert np.all(np.isnan(yv[:, 10])) and np.all(np.isnan(y64[:, 10]))
+        keep = np.ones(256, bool)
+        keep[10] = False
+        assert_close(y16[:, keep], y64[:, keep])
+
+
+# --------------------------------------------------- full-size workloads
+def sample_points(n, N, K, count, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    rows = np.concatenate([[0, 1, 127, 128, N - 129, N - 128, N - 1], rng.integers(0, N, count)])
+    toks = rng.integers(0, n, rows.shape[0])
+    return toks, rows
+
+
+@pytest.mark.parametrize("name,N,K,ns,outlier", [
+    ("attn_qkv", 14336, 5120, (1, 2, 3, 4), 0.0),
+    ("o_proj", 5120, 6144, (8,), 0.01),
+    ("fused_qkv", 16384, 5120, (16,), 0.0),
+])
+def test_full_size_workloads_sampled(name, N, K, ns, outlier):
+    w = synth.weights_f32(N, K, 0)
+    packed, scale, g = oracle.quantize(w)
+    nmax = max(ns)
+    x = synth.activations_bf16(nmax, K, 1, outlier)
+    wp, ws, gs, xt_all = to_gpu(packed, scale, g, x)
+    per_token = {}
+    for n in ns:
+        y = nv.nvfp4_gemv_batched(wp, ws, gs, xt_all[:n].contiguous())
+        torch.cuda.synchronize()
+        y16 = y.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert not np.isnan(bf16_to_f64(y16)).any()
+        toks, rows = sample_points(n, N, K, 400, 11 + n)
+        ref64, _ = oracle.gemv_points(packed, scale, g, x[:n], toks, rows)
+        assert_close(y16[toks, rows], ref64)
+        per_token[n] = y16
+    # batched == single token, bit for bit, on the full-size launch configuration
+    if 1 in per_token:
+        for n, y16 in per_token.items():
+            assert np.array_equal(y16[0], per_token[1][0])
+    else:
+        y1 = nv.nvfp4_gemv_batched(wp, ws, gs, xt_all[nmax - 1:nmax].contiguous())
+        torch.cuda.synchronize()
+        assert np.array_equal(y1.view(torch.int16).cpu().numpy().view(np.uint16)[0], per_token[nmax][nmax - 1])
+
+
+def test_no_device_error_recorded():
+    assert nv.nvfp4_device_error() == 0
