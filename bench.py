@@ -1,0 +1,461 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 batched decode GEMV on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload attn_qkv|o_proj|fused_qkv|decode_step] [--tiling one_pass|greedy_321]
+
+Prints ONE JSON line (rank 0).  A step is one pass of the hot path over one
+batch: for the default workload (attention qkv projection, N=14336, K=5120)
+that is four calls, n = 1, 2, 3 and 4 decode tokens, each on its own weight
+copy.  Sixteen rotated weight copies (661 MB) keep the working set above the
+129 MB L2, so every call streams its weights from HBM.  `value` is the
+whole-job algorithmic HBM throughput (packed weights + scales + activations,
+GB/s); per-n µs/call are reported beside it.  Steps are replayed from CUDA
+graphs and timed with CUDA events on the launching stream.
+
+`--impl reference` times the CPU oracle (oracle/, test infrastructure) on the
+host cores on a bounded sample of the same workload, in the same metric.
+With torchrun (--gpus N > 1) every rank runs an independent replica (the
+GEMV has no exchange step); rank 0 prints the max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import multiprocessing as mp
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "NVFP4 batched GEMV µs/call & HBM GB/s (frac of GB300 peak), n=1–16"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+COPIES = 16
+
+# workload -> list of (shape name, n) calls per step
+SHAPES = {"attn_qkv": (14336, 5120), "o_proj": (5120, 6144), "fused_qkv": (16384, 5120)}
+OUTLIER = {"attn_qkv": 0.0, "o_proj": 0.01, "fused_qkv": 0.0}
+
+
+def workload_calls(name: str, n_sweep: int):
+    if name == "attn_qkv":
+        return [("attn_qkv", n) for n in (1, 2, 3, 4)]
+    if name == "o_proj":
+        return [("o_proj", 8)]
+    if name == "fused_qkv":
+        return [("fused_qkv", 16)]
+    if name == "decode_step":
+        return [(s, n_sweep) for _ in range(16) for s in ("attn_qkv", "o_proj")]
+    raise SystemExit(f"unknown workload {name}")
+
+
+def call_bytes(shape: str, n: int) -> int:
+    """Algorithmic HBM bytes of one call: W (K/2 per row) + scales (K/16 per row) + X (2nK)."""
+    N, K = SHAPES[shape]
+    return N * K // 2 + N * K // 16 + 2 * n * K
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def stream_kernel_traffic():
+    """Per-launch DRAM bytes of the streaming kernel from the committed ncu summary,
+    if the kernel source is unchanged since those counters were taken."""
+    src = os.path.join(ROOT, "nvfp4_weight_quantized_gemv_gb300", "csrc", "gemv_stream.cu")
+    prof = os.path.join(ROOT, "profiles", "gemv_stream_mma_attn_qkv.md")
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        text = open(prof).read()
+    except OSError:
+        return None, None
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_tr = re.search(r"dram_bytes_per_launch_n(\d+):\s*([0-9]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != digest:
+        return None, None
+    return int(m_tr.group(2)), int(m_tr.group(1))
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"nvfp4_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), hw=parts[5], hwt=parts[6], swt=parts[7],
+                                 pcap=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("pcap", "sw_power_cap")):
+                if r[key].lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------ CPU oracle
+def _oracle_task(args):
+    packed, scale, g, x = args
+    import oracle
+    oracle.gemv_rows(packed, scale, g, x)
+    return packed.shape[0]
+
+
+def cpu_oracle_sample(calls, rows_per_core: int, cores: int, steps: int = 1):
+    """Time the CPU oracle on a bounded sample of one step of the workload.
+
+    For every call of the step, `rows_per_core * cores` output rows (all of the
+    call's tokens) are computed by the fp64 oracle, split over `cores` spawned
+    processes.  Inputs are drawn and quantized (by the oracle) in this process
+    before timing.  Returns (GB/s of the sampled algorithmic bytes, wall seconds
+    per step, description)."""
+    import oracle
+    oracle.build()
+    tasks, nbytes = [], 0
+    for ci, (shape, n) in enumerate(calls):
+        N, K = SHAPES[shape]
+        rows = min(N, rows_per_core * cores)
+        packed, scale, g = oracle.quantize(synth.weights_f32(rows, K, 1000 + ci))
+        x = synth.activations_bf16(n, K, 1, OUTLIER[shape])
+        per = -(-rows // cores)
+        for r0 in range(0, rows, per):
+            r1 = min(rows, r0 + per)
+            tasks.append((packed[r0:r1].copy(), scale[r0:r1].copy(), g, x))
+        nbytes += rows * (K // 2 + K // 16) + 2 * n * K
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        pool.map(_oracle_task, [(t[0][:1], t[1][:1], t[2], t[3]) for t in tasks[:cores]])  # warm workers
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            pool.map(_oracle_task, tasks, chunksize=1)
+        wall = (time.perf_counter() - t0) / steps
+    sample = (f"{rows_per_core * cores} output rows (all tokens) of each of the {len(calls)} calls of one step "
+              f"({', '.join(f'{s} n={n}' for s, n in calls[:4])}{'...' if len(calls) > 4 else ''}); fp64 oracle "
+              f"over {cores} spawned processes; GB/s of the sampled rows' weight+scale+activation bytes")
+    return nbytes / wall / 1e9, wall, sample
+
+
+# ------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="attn_qkv", choices=["attn_qkv", "o_proj", "fused_qkv", "decode_step"])
+    ap.add_argument("--n", type=int, default=8, help="tokens per call for --workload decode_step")
+    ap.add_argument("--tiling", default="one_pass", choices=["one_pass", "greedy_321"])
+    ap.add_argument("--variant", default="auto", choices=["auto", "mma", "simt", "generic"])
+    ap.add_argument("--cpu-rows", type=int, default=96, help="oracle sample rows per host core and call")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    calls = workload_calls(args.workload, args.n)
+    step_bytes = sum(call_bytes(s, n) for s, n in calls)
+    cores = os.cpu_count() or 1
+    wl_desc = {
+        "attn_qkv": "attention qkv projection N=14336 K=5120, n=1,2,3,4 (one call each per step)",
+        "o_proj": "output projection N=5120 K=6144, n=8, activations with 1% x20 outliers",
+        "fused_qkv": "fused projection N=16384 K=5120, n=16",
+        "decode_step": f"decode step: 16 x (qkv N=14336 K=5120, o_proj N=5120 K=6144), n={args.n}",
+    }[args.workload]
+
+    # ---------------------------------------------------- reference arm
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # each step is a bounded sample (cpu_rows rows per core of every call);
+        # the run is capped at 5 timed steps so it ends within a few minutes
+        steps_run = max(1, min(args.steps, 5))
+        cpu_oracle_sample(calls, max(1, args.cpu_rows // 8), cores, steps=1)  # warm-up sample
+        gbs, wall, sample = cpu_oracle_sample(calls, args.cpu_rows, cores, steps=steps_run)
+        line = {"metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
+                "steps": steps_run, "warmup": 1, "ms_per_step": round(wall * 1e3, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded PCG64: W~N(0,0.02) quantized to NVFP4, X~N(0,1) bf16)",
+                "config": {"workload": wl_desc, "tiling": "per token (each output computed on its own)",
+                           "sample_per_step": sample},
+                "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "gpu_launches": 0}
+        print(json.dumps(line), flush=True)
+        return
+
+    # ------------------------------------------------------------ our arm
+    import torch
+    import nvfp4_weight_quantized_gemv_gb300 as nv
+
+    nv.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.Stream()
+    variant = {"auto": nv.VARIANT_AUTO, "mma": nv.VARIANT_MMA, "simt": nv.VARIANT_SIMT,
+               "generic": nv.VARIANT_GENERIC}[args.variant]
+    tiling = nv.TILING_ONE_PASS if args.tiling == "one_pass" else nv.TILING_GREEDY_321
+
+    # weights: one host draw per shape, quantized by the library's host
+    # quantizer, then COPIES distinct device copies (rows rolled per copy)
+    shapes_used = sorted({s for s, _ in calls})
+    weights = {}
+    for si, s in enumerate(shapes_used):
+        N, K = SHAPES[s]
+        packed, scale, g = nv.nvfp4_quantize_ref(synth.weights_f32(N, K, 100 + si))
+        wp0 = torch.from_numpy(packed).to(dev)
+        ws0 = torch.from_numpy(scale).to(dev)
+        ncopies = COPIES if args.workload != "decode_step" else 16
+        copies = []
+        for c in range(ncopies):
+            copies.append((torch.roll(wp0, shifts=c * 97, dims=0).contiguous(),
+                           torch.roll(ws0, shifts=c * 97, dims=0).contiguous(),
+                           torch.tensor([g], dtype=torch.float32, device=dev)))
+        weights[s] = copies
+        del wp0, ws0
+    xs, ys, xs_host, ys_host = {}, {}, {}, {}
+    for s, n in calls:
+        if (s, n) in xs:
+            continue
+        N, K = SHAPES[s]
+        xh = synth.activations_bf16(n, K, 1, OUTLIER[s])
+        xs_host[(s, n)] = torch.from_numpy(xh.view(np.int16)).view(torch.bfloat16).pin_memory()
+        xs[(s, n)] = xs_host[(s, n)].to(dev)
+        ys[(s, n)] = torch.empty((n, N), dtype=torch.bfloat16, device=dev)
+        ys_host[(s, n)] = torch.empty((n, N), dtype=torch.bfloat16).pin_memory()
+
+    # Step p (p = 0..P-1) uses weight copies rotating so that consecutive
+    # calls never reuse a copy within 16 calls of each other.
+    counters = {s: 0 for s in shapes_used}
+
+    def enqueue_step(st):
+        for s, n in calls:
+            wp, ws, gs = weights[s][counters[s] % len(weights[s])]
+            counters[s] += 1
+            nv.nvfp4_gemv_batched_ex(wp, ws, gs, xs[(s, n)], ys[(s, n)], stream=st, variant=variant, tiling=tiling)
+
+    # warm the library (workspace for this stream, descriptors) outside capture
+    with torch.cuda.stream(stream):
+        enqueue_step(stream)
+    stream.synchronize()
+    per_step_calls = len(calls)
+    phases = max(1, min(16, max(len(w) for w in weights.values()) // max(1, per_step_calls)))
+    graphs = []
+    for _ in range(phases):
+        gph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gph, stream=stream):
+            enqueue_step(stream)
+        graphs.append(gph)
+    plan = nv.nvfp4_gemv_plan(calls[-1][1], *SHAPES[calls[-1][0]], variant=variant, tiling=tiling)
+    launches_per_step = sum(nv.nvfp4_gemv_plan(n, *SHAPES[s], variant=variant, tiling=tiling)["passes"]
+                            for s, n in calls)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % phases].replay()
+    stream.synchronize()
+    if nv.nvfp4_device_error(stream) != 0:
+        raise SystemExit("device error during warm-up")
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[i % phases].replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    if nv.nvfp4_device_error(stream) != 0:
+        raise SystemExit("device error during the timed region")
+
+    # per-call breakdown (each call shape timed alone, back-to-back graph replays)
+    per_call = {}
+    for s, n in dict.fromkeys(calls):
+        key = f"{s}_n{n}"
+        g1 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g1, stream=stream):
+            for c in range(len(weights[s])):
+                wp, ws, gs = weights[s][c]
+                nv.nvfp4_gemv_batched_ex(wp, ws, gs, xs[(s, n)], ys[(s, n)], stream=stream, variant=variant,
+                                         tiling=tiling)
+        reps = max(20, min(400, 40000 // len(weights[s])))
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g1.replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                g1.replay()
+            b.record(stream)
+        b.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (reps * len(weights[s]))
+        gbs = call_bytes(s, n) / (us * 1e-6) / 1e9
+        per_call[key] = {"us_per_call": round(us, 3), "GB_s": round(gbs, 1)}
+    hbm_peak, peak_kind = peaks()
+    for v in per_call.values():
+        v["frac_of_measured_hbm"] = round(v["GB_s"] / hbm_peak, 4)
+        v["frac_of_8TBs"] = round(v["GB_s"] / NOMINAL_HBM_GBS, 4)
+    if args.workload == "attn_qkv":
+        base = per_call["attn_qkv_n1"]["us_per_call"]
+        for v in per_call.values():
+            v["ratio_to_n1"] = round(v["us_per_call"] / base, 3)
+
+    # end to end through the public API with host buffers: every step copies
+    # the activations in from pinned host memory and the outputs back out
+    e2e_steps = max(20, min(2000, args.steps // 20))
+    h2d = sum(xs_host[(s, n)].numel() * 2 for s, n in calls)
+    d2h = sum(ys_host[(s, n)].numel() * 2 for s, n in calls)
+
+    def e2e_step():
+        for s, n in calls:
+            wp, ws, gs = weights[s][counters[s] % len(weights[s])]
+            counters[s] += 1
+            xs[(s, n)].copy_(xs_host[(s, n)], non_blocking=True)
+            nv.nvfp4_gemv_batched(wp, ws, gs, xs[(s, n)], ys[(s, n)], stream=stream)
+            ys_host[(s, n)].copy_(ys[(s, n)], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+        stream.synchronize()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+    b.synchronize()
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+
+    traffic, traffic_n = stream_kernel_traffic()
+    achieved = step_bytes / (ms_per_step * 1e-3) / 1e9  # per GPU: algorithmic bytes per launch / launch time
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s",
+                "frac_of_8TBs": round(achieved / NOMINAL_HBM_GBS, 4),
+                "kernel": f"gemv_stream_kernel<{plan['variant']}>",
+                "algorithmic_bytes_per_step": step_bytes,
+                "traffic_note": (f"ncu dram read+write bytes per launch at n={traffic_n}" if traffic else
+                                 "null: no ncu counters for the current kernel source")}
+
+    if dist is not None:
+        dist.barrier()
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        gbs, wall, sample = cpu_oracle_sample(calls if args.workload != "decode_step" else calls[:2],
+                                              args.cpu_rows, cores)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16*f16+f32 (nvfp4 weights, bf16 activations)",
+        "data": "synthetic (seeded PCG64: W~N(0,0.02) quantized to NVFP4, X~N(0,1) bf16)",
+        "config": {"workload": wl_desc, "tiling": args.tiling, "variant": plan["variant"],
+                   "weight_copies": len(weights[calls[0][0]]),
+                   "l2": "inputs larger than L2: weight copies rotated, no copy reused within 16 calls",
+                   "grid": plan["num_ctas"], "stages": plan["stages"], "parallelism": f"replicas x{world}"},
+        "per_call": per_call,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
