@@ -64,7 +64,7 @@ def lib():
         if _lib is None:
             if not os.path.exists(LIB_PATH):
                 raise RuntimeError(f"{LIB_PATH} is missing: build it with "
-                                   "`python -m nvfp4_weight_quantized_gemv_gb300.build`")
+                                   "`python -m nvfp4_weight_quantized_gemv_gb300.buildlib`")
             L = ctypes.CDLL(LIB_PATH)
             vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
             L.nvfp4_gemv_batched.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
@@ -200,5 +200,5 @@ def nvfp4_device_error(stream=None) -> int:
 
 
 def build(force: bool = False) -> str:
-    from .build import build as _build
+    from .buildlib import build as _build
     return _build(force=force)

@@ -1,6 +1,6 @@
 """Build the in-tree C-ABI library ``libnvfp4_gemv.so`` for sm_103a.
 
-Usage: ``python -m nvfp4_weight_quantized_gemv_gb300.build`` (or ``build()``).
+Usage: ``python -m nvfp4_weight_quantized_gemv_gb300.buildlib`` (or ``build()``).
 Translation units compile in parallel with nvcc, then link into one shared
 library next to this file.  Static cudart, one -gencode (compute_103a/sm_103a).
 """
