@@ -119,6 +119,31 @@ nvfp4_status nvfp4_gemv_batched_ex(const uint8_t *w_packed, const uint8_t *w_sca
                                    uint16_t *y_bf16, int n, int N, int K, cudaStream_t stream,
                                    const nvfp4_gemv_opts *opts);
 
+/*
+ * nvfp4_gemv_batched without any device allocation.  The pages have no
+ * counterpart: this entry point exists for callers that cannot call cudaMalloc
+ * -- engines that reserve nearly all device memory in their own pool up front
+ * (a library allocation would fail or fragment it), code that must not
+ * allocate once serving has started (cudaMalloc can synchronize the device),
+ * and plugins that only receive pointers from a host program owning all
+ * device memory.
+ * Arguments, layout, ownership and validation as nvfp4_gemv_batched; the
+ * caller still passes every input and output buffer.  The kernel's scratch
+ * (split-tile counters and fp32 partials) is a static device array inside the
+ * library sized for GPUs with up to 160 SMs (2,624,000 bytes, held by every
+ * GPU that loads the library until the process exits); a device with more SMs
+ * gets NVFP4_ERR_WORKSPACE.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current: make that
+ * first call before any stream capture.  Each call clears the counters with
+ * cudaMemsetAsync on `stream`.  All calls on a device share the array, so
+ * calls that can overlap on the GPU race and may return wrong results:
+ * serialize them (one stream), or use nvfp4_gemv_batched_ex with a workspace
+ * per stream.  Never calls cudaMalloc or cudaFree.
+ */
+nvfp4_status nvfp4_gemv_batched_noalloc(const uint8_t *w_packed, const uint8_t *w_scale_e4m3,
+                                        const float *w_global_scale_f32, const uint16_t *x_bf16,
+                                        uint16_t *y_bf16, int n, int N, int K, cudaStream_t stream);
+
 /* Bytes of device workspace a call with these options needs (opts may be NULL). */
 nvfp4_status nvfp4_gemv_workspace_size(int n, int N, int K, const nvfp4_gemv_opts *opts,
                                        size_t *bytes);

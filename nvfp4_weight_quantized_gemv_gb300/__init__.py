@@ -32,7 +32,8 @@ VARIANT_NAMES = {0: "auto", 1: "mma", 2: "simt", 3: "generic"}
 TILING_NAMES = {0: "auto", 1: "one_pass", 2: "greedy_321"}
 
 # Names the C ABI exports (include/nvfp4_gemv.h).
-EXPORTS = ("nvfp4_gemv_batched", "nvfp4_gemv_batched_ex", "nvfp4_gemv_workspace_size", "nvfp4_gemv_plan",
+EXPORTS = ("nvfp4_gemv_batched", "nvfp4_gemv_batched_ex", "nvfp4_gemv_batched_noalloc",
+           "nvfp4_gemv_workspace_size", "nvfp4_gemv_plan",
            "nvfp4_quantize_ref", "nvfp4_device_error", "nvfp4_last_error", "nvfp4_version")
 
 
@@ -71,6 +72,8 @@ def lib():
             L.nvfp4_gemv_batched.restype = i
             L.nvfp4_gemv_batched_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp, ctypes.POINTER(nvfp4_gemv_opts)]
             L.nvfp4_gemv_batched_ex.restype = i
+            L.nvfp4_gemv_batched_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
+            L.nvfp4_gemv_batched_noalloc.restype = i
             L.nvfp4_gemv_workspace_size.argtypes = [i, i, i, ctypes.POINTER(nvfp4_gemv_opts), ctypes.POINTER(sz)]
             L.nvfp4_gemv_workspace_size.restype = i
             L.nvfp4_gemv_plan.argtypes = [i, i, i, ctypes.POINTER(nvfp4_gemv_opts),
@@ -157,6 +160,17 @@ def nvfp4_gemv_batched_ex(w_packed, w_scale, w_global_scale, x, y=None, stream=N
     _check(lib().nvfp4_gemv_batched_ex(w_packed.data_ptr(), w_scale.data_ptr(), w_global_scale.data_ptr(),
                                        x.data_ptr(), y.data_ptr(), n, N, K, _stream_handle(stream),
                                        ctypes.byref(o)))
+    return y
+
+
+def nvfp4_gemv_batched_noalloc(w_packed, w_scale, w_global_scale, x, y, stream=None):
+    """Allocation-free variant for callers that cannot call cudaMalloc (see the C header).
+
+    `y` must be provided by the caller; the library allocates nothing.  Calls
+    that can overlap on the GPU share one scratch array and race."""
+    n, N, K = _gemv_args(w_packed, w_scale, w_global_scale, x, y)
+    _check(lib().nvfp4_gemv_batched_noalloc(w_packed.data_ptr(), w_scale.data_ptr(), w_global_scale.data_ptr(),
+                                            x.data_ptr(), y.data_ptr(), n, N, K, _stream_handle(stream)))
     return y
 
 
