@@ -58,7 +58,8 @@ typedef enum nvfp4_variant {
     NVFP4_VARIANT_AUTO = 0,
     NVFP4_VARIANT_MMA = 1,      /* TMA ring + register dequant + mma.sync f16 tensor cores */
     NVFP4_VARIANT_SIMT = 2,     /* TMA ring + register dequant + fp32 CUDA-core FMAs */
-    NVFP4_VARIANT_GENERIC = 3   /* plain loads, any K % 16 == 0 and any alignment */
+    NVFP4_VARIANT_GENERIC = 3,  /* plain loads, any K % 16 == 0 and any alignment */
+    NVFP4_VARIANT_TC = 4        /* TMA ring + dequant into tensor memory + tcgen05.mma (default) */
 } nvfp4_variant;
 
 /* Token tiling.  ONE_PASS streams W once for all n tokens (chunks of up to 16
@@ -89,7 +90,7 @@ typedef struct nvfp4_gemv_plan_info {
     int num_ctas;        /* grid size of each launch */
     int stages;          /* TMA ring stages */
     int smem_bytes;      /* dynamic shared memory per CTA */
-    long long units;     /* work units (128 rows x 128 k) per pass */
+    long long units;     /* work units (128 rows x 128 k; 128 x 256 for TC) per pass */
 } nvfp4_gemv_plan_info;
 
 /*
@@ -99,8 +100,11 @@ typedef struct nvfp4_gemv_plan_info {
  * y_bf16: device, written.  n >= 0 (n == 0 is a no-op), N >= 1, K >= 16 and
  * K % 16 == 0.  Any n is accepted; more than 16 tokens (or fewer when
  * n * K is too large for shared memory) are processed in chunks that each
- * re-read W.  The fast path needs K % 256 == 0 and 16-byte aligned w_packed,
- * w_scale_e4m3 and x_bf16; other inputs take the GENERIC kernel.
+ * re-read W.  The fast (tcgen05) path needs K % 256 == 0 and 16-byte aligned
+ * w_packed, w_scale_e4m3 and x_bf16; other inputs take the GENERIC kernel.
+ * The tcgen05 path scales X by 2^-8 before its f16 conversion, so entries with
+ * |x| >= 65520 * 2^8 (about 1.68e7) are out of range: they set the device
+ * error word (nvfp4_device_error) and the output is not meaningful.
  * Uses a library-owned workspace tied to `stream`, allocated on the first call
  * on that stream (make that first call before capturing `stream` in a graph).
  * Calls on different streams may run concurrently.
@@ -128,11 +132,11 @@ nvfp4_status nvfp4_gemv_batched_ex(const uint8_t *w_packed, const uint8_t *w_sca
  * and plugins that only receive pointers from a host program owning all
  * device memory.
  * Arguments, layout, ownership and validation as nvfp4_gemv_batched; the
- * caller still passes every input and output buffer.  The kernel's scratch
- * (split-tile counters and fp32 partials) is a static device array inside the
- * library sized for GPUs with up to 160 SMs (2,624,000 bytes, held by every
- * GPU that loads the library until the process exits); a device with more SMs
- * gets NVFP4_ERR_WORKSPACE.  The first call on a device looks up the array's
+ * caller still passes every input and output buffer.  The kernels' scratch
+ * (split-tile counters, fp32 partials, an f16 copy of X) is a static device array inside the
+ * library sized for GPUs with up to 160 SMs and K up to 65536 (4,723,712
+ * bytes, held by every GPU that loads the library until the process exits);
+ * a device with more SMs or a larger K gets NVFP4_ERR_WORKSPACE.  The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress) with that device current: make that
  * first call before any stream capture.  Each call clears the counters with
  * cudaMemsetAsync on `stream`.  All calls on a device share the array, so

@@ -26,9 +26,9 @@ NVFP4_ERR_DEVICE_TIMEOUT = 5
 NVFP4_ERR_WORKSPACE = 6
 
 # nvfp4_variant / nvfp4_tiling
-VARIANT_AUTO, VARIANT_MMA, VARIANT_SIMT, VARIANT_GENERIC = 0, 1, 2, 3
+VARIANT_AUTO, VARIANT_MMA, VARIANT_SIMT, VARIANT_GENERIC, VARIANT_TC = 0, 1, 2, 3, 4
 TILING_AUTO, TILING_ONE_PASS, TILING_GREEDY_321 = 0, 1, 2
-VARIANT_NAMES = {0: "auto", 1: "mma", 2: "simt", 3: "generic"}
+VARIANT_NAMES = {0: "auto", 1: "mma", 2: "simt", 3: "generic", 4: "tc"}
 TILING_NAMES = {0: "auto", 1: "one_pass", 2: "greedy_321"}
 
 # Names the C ABI exports (include/nvfp4_gemv.h).

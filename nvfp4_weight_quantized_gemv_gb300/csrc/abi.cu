@@ -77,6 +77,8 @@ static nvfp4_status device_state(int dev, DeviceState **out) {
                         d.major, d.minor);
         if ((e = stream_set_smem_limits(d.smem_optin)) != cudaSuccess)
             return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+        if ((e = tc_set_smem_limit(d.smem_optin)) != cudaSuccess)
+            return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory, tcgen05 kernel)");
         if ((e = device_error_word(&d.err_word)) != cudaSuccess)
             return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
         d.ready = true;
@@ -138,7 +140,7 @@ static nvfp4_status get_encode_fn(EncodeTiledFn *fn) {
 
 // 2D uint8 tensor [rows][cols] with row pitch `cols` bytes, box box_cols x box_rows.
 static nvfp4_status encode_2d(CUtensorMap *map, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                              uint32_t box_rows) {
+                              uint32_t box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
     EncodeTiledFn fn;
     nvfp4_status st = get_encode_fn(&fn);
     if (st != NVFP4_OK) return st;
@@ -147,7 +149,7 @@ static nvfp4_status encode_2d(CUtensorMap *map, const void *ptr, uint64_t cols, 
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
     return NVFP4_OK;
@@ -162,6 +164,7 @@ struct Plan {
     int stages = 0;
     int smem = 0;
     long long units = 0;
+    int tc_tokens = 0;  // tcgen05 kernel: tokens staged per pass (8 or 16)
 };
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -182,23 +185,28 @@ static nvfp4_status make_plan(int n, int N, int K, bool fast_ok, const nvfp4_gem
                               Plan *plan) {
     Plan p;
     p.variant = o.variant;
-    if (p.variant < kAuto || p.variant > kGeneric) return fail(NVFP4_ERR_INVALID_ARG, "unknown variant %d", o.variant);
-    if (o.tiling < NVFP4_TILING_AUTO || o.tiling > NVFP4_TILING_GREEDY_321)
-        return fail(NVFP4_ERR_INVALID_ARG, "unknown tiling %d", o.tiling);
-    if (p.variant == kAuto) p.variant = fast_ok ? kMma : kGeneric;
+    const bool tc_ok = fast_ok;
+    if (p.variant == kAuto) p.variant = tc_ok ? kTc : (fast_ok ? kMma : kGeneric);
     if ((p.variant == kMma || p.variant == kSimt) && !fast_ok)
         return fail(NVFP4_ERR_INVALID_ARG,
                     "variant %d needs K %% 256 == 0 and 16-byte aligned w_packed, w_scale_e4m3 and x_bf16",
                     p.variant);
+    if (p.variant == kTc && !tc_ok)
+        return fail(NVFP4_ERR_INVALID_ARG,
+                    "the tcgen05 variant needs K %% 256 == 0 and 16-byte aligned w_packed, w_scale_e4m3 and x_bf16");
     p.tiling = (o.tiling == NVFP4_TILING_AUTO) ? NVFP4_TILING_ONE_PASS : o.tiling;
 
     int per_pass = kMaxTokensPerPass;
-    if (p.variant != kGeneric) {
+    if (p.variant == kMma || p.variant == kSimt) {
         // largest token count whose X still leaves room for two ring stages
         const int room = smem_optin - stream_smem_bytes(2, 0, K);
         int fit = room / (2 * K);
         if (fit < 1) return fail(NVFP4_ERR_UNSUPPORTED, "K = %d too large for the streaming kernel", K);
         per_pass = fit < per_pass ? fit : per_pass;
+    } else if (p.variant == kTc) {
+        if (tc_smem_bytes(2, 16, K) <= smem_optin) per_pass = 16;
+        else if (tc_smem_bytes(2, 8, K) <= smem_optin) per_pass = 8;
+        else return fail(NVFP4_ERR_UNSUPPORTED, "K = %d too large for the tcgen05 kernel", K);
     }
     if (p.tiling == NVFP4_TILING_GREEDY_321) {
         p.tiles = greedy_321(n);
@@ -208,18 +216,22 @@ static nvfp4_status make_plan(int n, int N, int K, bool fast_ok, const nvfp4_gem
     if (p.variant != kGeneric) {
         int max_tile = 0;
         for (int t : p.tiles) max_tile = t > max_tile ? t : max_tile;
+        const int T = max_tile > 8 ? 16 : 8;
+        auto smem_for = [&](int st) {
+            return p.variant == kTc ? tc_smem_bytes(st, T, K) : stream_smem_bytes(st, max_tile, K);
+        };
         int stages = kMaxStages;
-        while (stages > 2 && stream_smem_bytes(stages, max_tile, K) > smem_optin) --stages;
+        while (stages > 2 && smem_for(stages) > smem_optin) --stages;
         if (o.stages != 0) {
-            if (o.stages < 2 || o.stages > kMaxStages)
-                return fail(NVFP4_ERR_INVALID_ARG, "stages must be 0 or 2..%d", kMaxStages);
             if (o.stages > stages)
                 return fail(NVFP4_ERR_INVALID_ARG, "stages = %d does not fit shared memory (max %d)", o.stages, stages);
             stages = o.stages;
         }
         p.stages = stages;
-        p.smem = stream_smem_bytes(stages, max_tile, K);
-        p.units = (long long)((N + kUnitRows - 1) / kUnitRows) * (K / kUnitK);
+        p.smem = smem_for(stages);
+        p.tc_tokens = p.variant == kTc ? T : 0;
+        const int unit_k = p.variant == kTc ? kTcUnitKHost : kUnitK;
+        p.units = (long long)((N + kUnitRows - 1) / kUnitRows) * (K / unit_k);
         int ctas = o.num_ctas ? o.num_ctas : sms;
         if (ctas < 1 || ctas > sms) return fail(NVFP4_ERR_INVALID_ARG, "num_ctas must be 0 or 1..%d", sms);
         if ((long long)ctas > p.units) ctas = (int)p.units;
@@ -240,7 +252,7 @@ static nvfp4_status validate(const void *wp, const void *ws, const void *gs, con
 }
 
 static nvfp4_status validate_opts(const nvfp4_gemv_opts &o) {
-    if (o.variant < kAuto || o.variant > kGeneric) return fail(NVFP4_ERR_INVALID_ARG, "unknown variant %d", o.variant);
+    if (o.variant < kAuto || o.variant > kTc) return fail(NVFP4_ERR_INVALID_ARG, "unknown variant %d", o.variant);
     if (o.tiling < NVFP4_TILING_AUTO || o.tiling > NVFP4_TILING_GREEDY_321)
         return fail(NVFP4_ERR_INVALID_ARG, "unknown tiling %d", o.tiling);
     if (o.num_ctas < 0) return fail(NVFP4_ERR_INVALID_ARG, "num_ctas = %d must be >= 0", o.num_ctas);
@@ -287,7 +299,8 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
     }
 
     // streaming kernels: workspace, descriptors, one launch per token tile
-    const size_t ws_bytes = stream_workspace_bytes(d->sms);
+    const size_t fixed_bytes = stream_workspace_bytes(d->sms);
+    const size_t ws_bytes = fixed_bytes + (plan.variant == kTc ? tc_xbuf_bytes(K) : 0);
     void *work = o.workspace;
     if (work) {
         if (o.workspace_bytes < ws_bytes)
@@ -298,19 +311,26 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
         return st;
     }
     CUtensorMap tw, ts;
-    if ((st = encode_2d(&tw, wp, (uint64_t)K / 2, (uint64_t)N, kUnitK / 2, kUnitRows)) != NVFP4_OK) return st;
+    if (plan.variant == kTc) {
+        if ((st = encode_2d(&tw, wp, (uint64_t)K / 2, (uint64_t)N, 128, kUnitRows, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+            NVFP4_OK)
+            return st;
+    } else if ((st = encode_2d(&tw, wp, (uint64_t)K / 2, (uint64_t)N, kUnitK / 2, kUnitRows)) != NVFP4_OK) {
+        return st;
+    }
     if ((st = encode_2d(&ts, ws, (uint64_t)K / 16, (uint64_t)N, 16, kUnitRows)) != NVFP4_OK) return st;
 
     StreamParams sp;
     sp.gscale = gs;
     sp.counters = static_cast<unsigned *>(work);
     sp.partials = reinterpret_cast<float *>(static_cast<char *>(work) + stream_counter_bytes(d->sms));
+    sp.xf16 = reinterpret_cast<const uint16_t *>(static_cast<char *>(work) + fixed_bytes);
     sp.err = d->err_word;
     sp.units = plan.units;
     sp.ctas = plan.ctas;
     sp.N = N;
     sp.K = K;
-    sp.KC = K / kUnitK;
+    sp.KC = K / (plan.variant == kTc ? kTcUnitKHost : kUnitK);
     sp.stages = plan.stages;
     int t0 = 0;
     for (int tn : plan.tiles) {
@@ -318,8 +338,9 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
         sp.y = y + (size_t)t0 * N;
         sp.n = tn;
         sp.y_vec2 = (N % 2 == 0) && ((reinterpret_cast<uintptr_t>(sp.y) & 3u) == 0);
-        if ((e = launch_stream(plan.variant, tw, ts, sp, plan.smem, stream)) != cudaSuccess)
-            return cuda_fail(e, "streaming kernel launch");
+        e = plan.variant == kTc ? launch_tc(tw, ts, sp, plan.tc_tokens, plan.smem, stream)
+                                : launch_stream(plan.variant, tw, ts, sp, plan.smem, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "streaming kernel launch");
         t0 += tn;
     }
     return NVFP4_OK;
@@ -369,7 +390,8 @@ extern "C" nvfp4_status nvfp4_gemv_workspace_size(int n, int N, int K, const nvf
     int sms = 0;
     nvfp4_status st = plan_host(n, N, K, opts, &plan, &sms);
     if (st != NVFP4_OK) return st;
-    *bytes = plan.variant == kGeneric ? 0 : stream_workspace_bytes(sms);
+    *bytes = plan.variant == kGeneric ? 0
+                                      : stream_workspace_bytes(sms) + (plan.variant == kTc ? tc_xbuf_bytes(K) : 0);
     return NVFP4_OK;
 }
 

@@ -9,10 +9,11 @@
 // entry point allocates a small workspace on the first call per stream; this
 // one never does.
 //
-// How: the streaming kernel's split-tile scratch (counters + fp32 partial
-// tiles) lives in the file-scope device array below, sized for grids of up to
-// kNoAllocMaxCtas CTAs (2.5 MB, held by every GPU that loads the library
-// until the process exits).  Its device address comes from
+// How: the kernels' scratch (split-tile counters, fp32 partial tiles and the
+// f16 copy of X that the tensor-core path streams) lives in the file-scope
+// device array below, sized for grids of up to kNoAllocMaxCtas CTAs and K up
+// to kNoAllocMaxK (4.5 MB, held by every GPU that loads the library until the
+// process exits).  Its device address comes from
 // cudaGetSymbolAddress, taken once per device with that device current, on
 // the first call on that device.  Each call then clears the counters with
 // cudaMemsetAsync on the caller's stream and runs the ordinary streaming path
@@ -36,11 +37,13 @@ void set_last_error(const char *msg);
 namespace {
 
 constexpr int kNoAllocMaxCtas = 160;
+constexpr int kNoAllocMaxK = 65536;
 // counters (rounded up to 256 bytes) + fp32 partial tiles, the layout of
-// stream_workspace_bytes(kNoAllocMaxCtas): 2,624,000 bytes
+// stream_workspace_bytes(kNoAllocMaxCtas), then X as f16 for 16 tokens x
+// kNoAllocMaxK (tc_xbuf_bytes): 2,626,560 + 2,097,152 = 4,723,712 bytes
 constexpr size_t kNoAllocScratchBytes =
-    (((size_t)kNoAllocMaxCtas * kConsumerWarps * sizeof(unsigned) + 255) & ~(size_t)255) +
-    (size_t)kNoAllocMaxCtas * 2 * kConsumerWarps * kSlotFloats * sizeof(float);
+    (((size_t)kNoAllocMaxCtas * kCountersPerCta * sizeof(unsigned) + 255) & ~(size_t)255) +
+    (size_t)kNoAllocMaxCtas * 2 * kConsumerWarps * kSlotFloats * sizeof(float) + (size_t)kNoAllocMaxK * 16 * 2;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -76,7 +79,13 @@ extern "C" nvfp4_status nvfp4_gemv_batched_noalloc(const uint8_t *w_packed, cons
     int sms = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return noalloc_fail(NVFP4_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
-    const size_t needed = stream_workspace_bytes(sms);
+    if (K > kNoAllocMaxK) {
+        char buf[160];
+        std::snprintf(buf, sizeof buf, "nvfp4_gemv_batched_noalloc: K = %d exceeds the static scratch's limit of %d",
+                      K, kNoAllocMaxK);
+        return noalloc_fail(NVFP4_ERR_WORKSPACE, buf);
+    }
+    const size_t needed = stream_workspace_bytes(sms) + tc_xbuf_bytes(K);
     if (needed > kNoAllocScratchBytes) {
         char buf[256];
         std::snprintf(buf, sizeof buf,

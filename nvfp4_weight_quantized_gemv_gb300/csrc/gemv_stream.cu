@@ -267,7 +267,7 @@ __device__ __forceinline__ void flush_tile(const StreamParams &p, float (&v)[16]
         __threadfence();
         __syncwarp();
         unsigned old = 0;
-        if (lane == 0) old = atomicAdd(&p.counters[cfirst * kConsumerWarps + warp], 1u);
+        if (lane == 0) old = atomicAdd(&p.counters[cfirst * kCountersPerCta + warp], 1u);
         old = __shfl_sync(0xffffffffu, old, 0);
         if (old != (unsigned)(clast - cfirst)) return;  // another CTA finishes this tile
         __threadfence();
@@ -285,7 +285,7 @@ __device__ __forceinline__ void flush_tile(const StreamParams &p, float (&v)[16]
                 }
             }
         }
-        if (lane == 0) atomicExch(&p.counters[cfirst * kConsumerWarps + warp], 0u);
+        if (lane == 0) atomicExch(&p.counters[cfirst * kCountersPerCta + warp], 0u);
     }
     epilogue<kVariant>(p, v, row_base, lane, gs);
 }

@@ -76,21 +76,26 @@ def test_greedy_321_tiling_matches_the_pages():
 def test_one_pass_plan():
     for n in (1, 4, 8, 16):
         plan = nv.nvfp4_gemv_plan(n, 14336, 5120)
-        assert plan["variant"] == "mma" and plan["tiling"] == "one_pass"
+        assert plan["variant"] == "tc" and plan["tiling"] == "one_pass"
         assert plan["passes"] == 1 and plan["tile_tokens"] == [n]
-        assert plan["units"] == (14336 // 128) * (5120 // 128)
+        assert plan["units"] == (14336 // 128) * (5120 // 256)
+        mma = nv.nvfp4_gemv_plan(n, 14336, 5120, variant=nv.VARIANT_MMA)
+        assert mma["units"] == (14336 // 128) * (5120 // 128)
         assert 2 <= plan["stages"] <= 8 and plan["smem_bytes"] <= 232448
     # more than 16 tokens: chunks of 16
     assert nv.nvfp4_gemv_plan(20, 4096, 4096)["tile_tokens"] == [16, 4]
     # K too large for 16 tokens of X in shared memory: smaller chunks
     p = nv.nvfp4_gemv_plan(16, 1024, 8192)
+    assert p["tile_tokens"] == [16]        # tcgen05: X is streamed per unit, any K fits
+    p = nv.nvfp4_gemv_plan(16, 1024, 8192, variant=nv.VARIANT_MMA)
     assert sum(p["tile_tokens"]) == 16 and max(p["tile_tokens"]) < 16
     # K % 256 != 0 -> generic kernel, no workspace
     assert nv.nvfp4_gemv_plan(3, 100, 784)["variant"] == "generic"
     assert nv.nvfp4_gemv_workspace_size(3, 100, 784) == 0
     assert nv.nvfp4_gemv_workspace_size(3, 14336, 5120) > 0
     # the grid never exceeds the number of units
-    assert nv.nvfp4_gemv_plan(3, 256, 512)["num_ctas"] == 2 * 4
+    assert nv.nvfp4_gemv_plan(3, 256, 512)["num_ctas"] == 2 * 2          # tcgen05: 128 x 256 units
+    assert nv.nvfp4_gemv_plan(3, 256, 512, variant=nv.VARIANT_MMA)["num_ctas"] == 2 * 4
 
 
 def test_host_quantizer_matches_oracle_bytes():

@@ -17,7 +17,7 @@ import synth
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-2
-VARIANTS = {"mma": nv.VARIANT_MMA, "simt": nv.VARIANT_SIMT, "generic": nv.VARIANT_GENERIC}
+VARIANTS = {"tc": nv.VARIANT_TC, "mma": nv.VARIANT_MMA, "simt": nv.VARIANT_SIMT, "generic": nv.VARIANT_GENERIC}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -72,7 +72,7 @@ def test_tiny_workload_full_output(variant, tiling):
 
 
 @pytest.mark.parametrize("variant", list(VARIANTS))
-@pytest.mark.parametrize("N,K,n", [(1000, 1024, 5), (200, 512, 16), (129, 256, 9), (1, 256, 1), (384, 2048, 8)])
+@pytest.mark.parametrize("N,K,n", [(1000, 1024, 5), (200, 512, 16), (129, 256, 9), (1, 256, 1), (384, 2048, 8), (256, 8192, 16)])
 def test_ragged_shapes_full_output(variant, N, K, n):
     packed, scale, g, x = make_case(N, K, n, 3, 4, outlier=0.01)
     y64, _ = oracle.gemv(packed, scale, g, x)
@@ -84,7 +84,7 @@ def test_one_hot_pins_nibble_order_and_scale_placement():
     """Single-term outputs are exact: y[t, r] = bf16(E2M1 * E4M3 * g) at k_t."""
     N, K = 128, 256
     packed, scale, g, _ = make_case(N, K, 1, 9, 0)
-    for variant in ("mma", "simt"):
+    for variant in ("tc", "mma", "simt"):
         for k0 in range(0, K, 16):
             x = np.zeros((16, K), dtype=np.uint16)
             x[np.arange(16), k0 + np.arange(16)] = 0x3F80
@@ -114,11 +114,12 @@ def test_repeat_calls_are_bit_identical():
         assert np.array_equal(gpu_gemv(dev), first)
 
 
+@pytest.mark.parametrize("variant", ["tc", "mma"])
 @pytest.mark.parametrize("num_ctas,stages", [(1, 2), (3, 0), (7, 3), (0, 2), (150, 8)])
-def test_grid_and_ring_options(num_ctas, stages):
+def test_grid_and_ring_options(variant, num_ctas, stages):
     packed, scale, g, x = make_case(700, 1280, 4, 7, 8)
     y64, _ = oracle.gemv(packed, scale, g, x)
-    y16 = gpu_gemv(to_gpu(packed, scale, g, x), nv.VARIANT_MMA, num_ctas=num_ctas, stages=stages)
+    y16 = gpu_gemv(to_gpu(packed, scale, g, x), VARIANTS[variant], num_ctas=num_ctas, stages=stages)
     assert_close(y16, y64)
 
 
@@ -186,7 +187,7 @@ def test_activation_beyond_f16_range_is_rescaled():
     xf[2, 900] = -1.0e6
     x = synth.to_bf16_bits(xf)
     y64, _ = oracle.gemv(packed, scale, g, x)
-    for variant in ("mma", "simt", "generic"):
+    for variant in ("tc", "mma", "simt", "generic"):
         assert_close(gpu_gemv(to_gpu(packed, scale, g, x), VARIANTS[variant]), y64)
 
 
