@@ -76,11 +76,21 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def stream_kernel_traffic():
-    """Per-launch DRAM bytes of the streaming kernel from the committed ncu summary,
+# variant -> (kernel source, committed ncu summary, kernel name)
+KERNELS = {
+    "tc": ("gemv_tc.cu", "gemv_tc_attn_qkv.md", "gemv_tc_kernel"),
+    "mma": ("gemv_stream.cu", "gemv_stream_mma_attn_qkv.md", "gemv_stream_kernel<mma>"),
+    "simt": ("gemv_stream.cu", "gemv_stream_simt_attn_qkv.md", "gemv_stream_kernel<simt>"),
+    "generic": ("gemv_generic.cu", "gemv_generic_attn_qkv.md", "gemv_generic_kernel"),
+}
+
+
+def kernel_traffic(variant):
+    """Per-launch DRAM bytes of the variant's kernel from the committed ncu summary,
     if the kernel source is unchanged since those counters were taken."""
-    src = os.path.join(ROOT, "nvfp4_weight_quantized_gemv_gb300", "csrc", "gemv_stream.cu")
-    prof = os.path.join(ROOT, "profiles", "gemv_stream_mma_attn_qkv.md")
+    src_name, prof_name, _ = KERNELS[variant]
+    src = os.path.join(ROOT, "nvfp4_weight_quantized_gemv_gb300", "csrc", src_name)
+    prof = os.path.join(ROOT, "profiles", prof_name)
     try:
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
         text = open(prof).read()
@@ -411,14 +421,14 @@ def main():
         e2e_ms = float(t.item())
     e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
 
-    traffic, traffic_n = stream_kernel_traffic()
+    traffic, traffic_n = kernel_traffic(plan["variant"])
     achieved = step_bytes / (ms_per_step * 1e-3) / 1e9  # per GPU: algorithmic bytes per launch / launch time
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                 "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
                 "frac_of_8TBs": round(achieved / NOMINAL_HBM_GBS, 4),
-                "kernel": f"gemv_stream_kernel<{plan['variant']}>",
+                "kernel": KERNELS[plan["variant"]][2],
                 "algorithmic_bytes_per_step": step_bytes,
                 "traffic_note": (f"ncu dram read+write bytes per launch at n={traffic_n}" if traffic else
                                  "null: no ncu counters for the current kernel source")}

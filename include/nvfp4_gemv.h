@@ -105,6 +105,12 @@ typedef struct nvfp4_gemv_plan_info {
  * The tcgen05 path scales X by 2^-8 before its f16 conversion, so entries with
  * |x| >= 65520 * 2^8 (about 1.68e7) are out of range: they set the device
  * error word (nvfp4_device_error) and the output is not meaningful.
+ * The tcgen05 kernel is launched with programmatic dependent launch: when the
+ * kernel ahead of it on `stream` allows its dependents to start early, the
+ * GEMV begins reading w_packed and w_scale_e4m3 before that kernel finishes
+ * (it reads x_bf16 and w_global_scale_f32 and writes y_bf16 only after).  So
+ * the weights must not be written by the kernel launched just before the call
+ * unless that kernel signals completion only at its end (the default).
  * Uses a library-owned workspace tied to `stream`, allocated on the first call
  * on that stream (make that first call before capturing `stream` in a graph).
  * Calls on different streams may run concurrently.
@@ -133,10 +139,10 @@ nvfp4_status nvfp4_gemv_batched_ex(const uint8_t *w_packed, const uint8_t *w_sca
  * device memory.
  * Arguments, layout, ownership and validation as nvfp4_gemv_batched; the
  * caller still passes every input and output buffer.  The kernels' scratch
- * (split-tile counters, fp32 partials, an f16 copy of X) is a static device array inside the
- * library sized for GPUs with up to 160 SMs and K up to 65536 (4,723,712
- * bytes, held by every GPU that loads the library until the process exits);
- * a device with more SMs or a larger K gets NVFP4_ERR_WORKSPACE.  The first call on a device looks up the array's
+ * (split-tile counters and fp32 partial tiles) is a static device array
+ * inside the library of 8 MiB (8,388,608 bytes, held by every GPU that loads
+ * the library until the process exits); a call whose plan needs more scratch
+ * than that (nvfp4_gemv_workspace_size) gets NVFP4_ERR_WORKSPACE.  The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress) with that device current: make that
  * first call before any stream capture.  Each call clears the counters with
  * cudaMemsetAsync on `stream`.  All calls on a device share the array, so

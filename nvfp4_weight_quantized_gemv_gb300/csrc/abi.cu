@@ -155,6 +155,25 @@ static nvfp4_status encode_2d(CUtensorMap *map, const void *ptr, uint64_t cols, 
     return NVFP4_OK;
 }
 
+// The f16 copy of X of one pass for the tcgen05 kernel, viewed as 3D {64 k,
+// n tokens, K/64 k-chunks} (token stride 2K bytes, chunk stride 128 bytes) so
+// that one box {64, T, 4} is one unit's X in the tensor core's
+// 128-byte-swizzled K-major layout; tokens past n read as zeros.
+static nvfp4_status encode_x(CUtensorMap *map, const uint16_t *x, int n, int K, int T) {
+    EncodeTiledFn fn;
+    nvfp4_status st = get_encode_fn(&fn);
+    if (st != NVFP4_OK) return st;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)n, (cuuint64_t)K / 64};
+    const cuuint64_t strides[2] = {(cuuint64_t)K * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)T, 4};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t *>(x), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled (X) failed (CUresult %d)", (int)r);
+    return NVFP4_OK;
+}
+
 // ------------------------------------------------------------------ policy
 struct Plan {
     int variant = kAuto;
@@ -165,7 +184,65 @@ struct Plan {
     int smem = 0;
     long long units = 0;
     int tc_tokens = 0;  // tcgen05 kernel: tokens staged per pass (8 or 16)
+    TcPartition part{};  // tcgen05 kernel: k-groups and their CTAs
+    size_t counter_bytes = 0, ws_bytes = 0;
 };
+
+// Largest k-group (unit columns) whose X for 16 tokens fits next to eight
+// weight stages; the partition uses it for every n, so results do not depend
+// on n.
+static int tc_group_limit(int smem_optin) {
+    int kg = 32;
+    while (kg > 1 && tc_smem_bytes(kMaxStages, 16, kg) > smem_optin) --kg;
+    return kg;
+}
+
+// Split K into k-groups and the grid into per-group CTA ranges (each group
+// gets CTAs in proportion to its units, at least one), and count the row
+// blocks any CTA touches.
+static nvfp4_status tc_partition(int N, int K, int ctas, int smem_optin, TcPartition *out, int *kg_max_out) {
+    TcPartition t{};
+    const int KC = K / kTcUnitKHost;
+    t.row_blocks = (N + kUnitRows - 1) / kUnitRows;
+    const int limit = tc_group_limit(smem_optin);
+    t.groups = (KC + limit - 1) / limit;
+    if (t.groups > kTcMaxGroups)
+        return fail(NVFP4_ERR_UNSUPPORTED, "K = %d needs %d k-groups (at most %d)", K, t.groups, kTcMaxGroups);
+    if (ctas < t.groups)
+        return fail(NVFP4_ERR_INVALID_ARG, "num_ctas = %d: the tcgen05 kernel needs at least %d CTAs for K = %d", ctas,
+                    t.groups, K);
+    std::vector<long long> units(t.groups);
+    std::vector<int> c(t.groups, 1);
+    for (int g = 0; g < t.groups; ++g) {
+        int ks, kg;
+        tc_group_host(g, t.groups, KC, &ks, &kg);
+        units[g] = (long long)t.row_blocks * kg;
+    }
+    for (int extra = ctas - t.groups; extra > 0; --extra) {
+        int best = -1;  // the group with the most units per CTA that can still take a CTA
+        for (int g = 0; g < t.groups; ++g) {
+            if (c[g] >= units[g]) continue;
+            if (best < 0 || units[g] * c[best] > units[best] * c[g]) best = g;
+        }
+        if (best < 0) break;
+        ++c[best];
+    }
+    t.cstart[0] = 0;
+    for (int g = 0; g < t.groups; ++g) t.cstart[g + 1] = t.cstart[g] + c[g];
+    t.max_seg = 1;
+    for (int g = 0; g < t.groups; ++g) {
+        int ks, kg;
+        tc_group_host(g, t.groups, KC, &ks, &kg);
+        for (int cl = 0; cl < c[g]; ++cl) {
+            const long long u0 = (long long)cl * units[g] / c[g], u1 = (long long)(cl + 1) * units[g] / c[g];
+            const int segs = (int)((u1 - 1) / kg - u0 / kg + 1);
+            if (segs > t.max_seg) t.max_seg = segs;
+        }
+    }
+    *out = t;
+    *kg_max_out = (KC + t.groups - 1) / t.groups;
+    return NVFP4_OK;
+}
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -203,11 +280,7 @@ static nvfp4_status make_plan(int n, int N, int K, bool fast_ok, const nvfp4_gem
         int fit = room / (2 * K);
         if (fit < 1) return fail(NVFP4_ERR_UNSUPPORTED, "K = %d too large for the streaming kernel", K);
         per_pass = fit < per_pass ? fit : per_pass;
-    } else if (p.variant == kTc) {
-        if (tc_smem_bytes(2, 16, K) <= smem_optin) per_pass = 16;
-        else if (tc_smem_bytes(2, 8, K) <= smem_optin) per_pass = 8;
-        else return fail(NVFP4_ERR_UNSUPPORTED, "K = %d too large for the tcgen05 kernel", K);
-    }
+    }  // tcgen05: 16 tokens per pass for any K (X is held per k-group)
     if (p.tiling == NVFP4_TILING_GREEDY_321) {
         p.tiles = greedy_321(n);
     } else {
@@ -217,25 +290,41 @@ static nvfp4_status make_plan(int n, int N, int K, bool fast_ok, const nvfp4_gem
         int max_tile = 0;
         for (int t : p.tiles) max_tile = t > max_tile ? t : max_tile;
         const int T = max_tile > 8 ? 16 : 8;
-        auto smem_for = [&](int st) {
-            return p.variant == kTc ? tc_smem_bytes(st, T, K) : stream_smem_bytes(st, max_tile, K);
-        };
-        int stages = kMaxStages;
-        while (stages > 2 && smem_for(stages) > smem_optin) --stages;
-        if (o.stages != 0) {
-            if (o.stages > stages)
-                return fail(NVFP4_ERR_INVALID_ARG, "stages = %d does not fit shared memory (max %d)", o.stages, stages);
-            stages = o.stages;
-        }
-        p.stages = stages;
-        p.smem = smem_for(stages);
-        p.tc_tokens = p.variant == kTc ? T : 0;
         const int unit_k = p.variant == kTc ? kTcUnitKHost : kUnitK;
         p.units = (long long)((N + kUnitRows - 1) / kUnitRows) * (K / unit_k);
         int ctas = o.num_ctas ? o.num_ctas : sms;
         if (ctas < 1 || ctas > sms) return fail(NVFP4_ERR_INVALID_ARG, "num_ctas must be 0 or 1..%d", sms);
         if ((long long)ctas > p.units) ctas = (int)p.units;
         p.ctas = ctas;
+        int kg_max = 0;
+        if (p.variant == kTc) {
+            nvfp4_status st = tc_partition(N, K, ctas, smem_optin, &p.part, &kg_max);
+            if (st != NVFP4_OK) return st;
+        }
+        auto smem_for = [&](int st) {
+            return p.variant == kTc ? tc_smem_bytes(st, T, kg_max) : stream_smem_bytes(st, max_tile, K);
+        };
+        // the tcgen05 kernel needs an even number of stages (every consumer warp
+        // waits on every phase of a stage's barriers)
+        const int stage_step = p.variant == kTc ? 2 : 1;
+        int stages = kMaxStages;
+        while (stages > 2 && smem_for(stages) > smem_optin) stages -= stage_step;
+        if (smem_for(stages) > smem_optin) return fail(NVFP4_ERR_UNSUPPORTED, "K = %d does not fit shared memory", K);
+        if (o.stages != 0) {
+            if (o.stages > stages)
+                return fail(NVFP4_ERR_INVALID_ARG, "stages = %d does not fit shared memory (max %d)", o.stages, stages);
+            if (o.stages % stage_step != 0)
+                return fail(NVFP4_ERR_INVALID_ARG, "stages = %d: the tcgen05 kernel needs an even number", o.stages);
+            stages = o.stages;
+        }
+        p.stages = stages;
+        p.smem = smem_for(stages);
+        p.tc_tokens = p.variant == kTc ? T : 0;
+        p.counter_bytes = ws_counter_bytes(sms, (N + kUnitRows - 1) / kUnitRows);
+        p.ws_bytes = p.counter_bytes + (p.variant == kTc ? (size_t)ctas * p.part.max_seg * kConsumerWarps *
+                                                                   kSlotFloats * sizeof(float) +
+                                                               tc_xbuf_bytes(K)
+                                                         : stream_partial_bytes(sms));
     }
     *plan = p;
     return NVFP4_OK;
@@ -299,8 +388,7 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
     }
 
     // streaming kernels: workspace, descriptors, one launch per token tile
-    const size_t fixed_bytes = stream_workspace_bytes(d->sms);
-    const size_t ws_bytes = fixed_bytes + (plan.variant == kTc ? tc_xbuf_bytes(K) : 0);
+    const size_t ws_bytes = plan.ws_bytes;
     void *work = o.workspace;
     if (work) {
         if (o.workspace_bytes < ws_bytes)
@@ -323,8 +411,7 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
     StreamParams sp;
     sp.gscale = gs;
     sp.counters = static_cast<unsigned *>(work);
-    sp.partials = reinterpret_cast<float *>(static_cast<char *>(work) + stream_counter_bytes(d->sms));
-    sp.xf16 = reinterpret_cast<const uint16_t *>(static_cast<char *>(work) + fixed_bytes);
+    sp.partials = reinterpret_cast<float *>(static_cast<char *>(work) + plan.counter_bytes);
     sp.err = d->err_word;
     sp.units = plan.units;
     sp.ctas = plan.ctas;
@@ -338,8 +425,14 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
         sp.y = y + (size_t)t0 * N;
         sp.n = tn;
         sp.y_vec2 = (N % 2 == 0) && ((reinterpret_cast<uintptr_t>(sp.y) & 3u) == 0);
-        e = plan.variant == kTc ? launch_tc(tw, ts, sp, plan.tc_tokens, plan.smem, stream)
-                                : launch_stream(plan.variant, tw, ts, sp, plan.smem, stream);
+        if (plan.variant == kTc) {
+            uint16_t *xf = reinterpret_cast<uint16_t *>(static_cast<char *>(work) + plan.ws_bytes - tc_xbuf_bytes(K));
+            CUtensorMap tx;
+            if ((st = encode_x(&tx, xf, tn, K, plan.tc_tokens)) != NVFP4_OK) return st;
+            e = launch_tc(tw, ts, tx, sp, plan.part, plan.tc_tokens, plan.smem, xf, stream);
+        } else {
+            e = launch_stream(plan.variant, tw, ts, sp, plan.smem, stream);
+        }
         if (e != cudaSuccess) return cuda_fail(e, "streaming kernel launch");
         t0 += tn;
     }
@@ -390,10 +483,21 @@ extern "C" nvfp4_status nvfp4_gemv_workspace_size(int n, int N, int K, const nvf
     int sms = 0;
     nvfp4_status st = plan_host(n, N, K, opts, &plan, &sms);
     if (st != NVFP4_OK) return st;
-    *bytes = plan.variant == kGeneric ? 0
-                                      : stream_workspace_bytes(sms) + (plan.variant == kTc ? tc_xbuf_bytes(K) : 0);
+    *bytes = plan.variant == kGeneric ? 0 : plan.ws_bytes;
     return NVFP4_OK;
 }
+
+namespace nvfp4 {
+int workspace_layout(int n, int N, int K, const void *opts, size_t *counter_bytes, size_t *total_bytes) {
+    Plan plan;
+    int sms = 0;
+    nvfp4_status st = plan_host(n, N, K, static_cast<const nvfp4_gemv_opts *>(opts), &plan, &sms);
+    if (st != NVFP4_OK) return st;
+    *counter_bytes = plan.variant == kGeneric ? 0 : plan.counter_bytes;
+    *total_bytes = plan.variant == kGeneric ? 0 : plan.ws_bytes;
+    return NVFP4_OK;
+}
+}  // namespace nvfp4
 
 extern "C" nvfp4_status nvfp4_gemv_plan(int n, int N, int K, const nvfp4_gemv_opts *opts,
                                         nvfp4_gemv_plan_info *info) {

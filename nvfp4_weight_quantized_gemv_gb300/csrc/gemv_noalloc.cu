@@ -9,11 +9,10 @@
 // entry point allocates a small workspace on the first call per stream; this
 // one never does.
 //
-// How: the kernels' scratch (split-tile counters, fp32 partial tiles and the
-// f16 copy of X that the tensor-core path streams) lives in the file-scope
-// device array below, sized for grids of up to kNoAllocMaxCtas CTAs and K up
-// to kNoAllocMaxK (4.5 MB, held by every GPU that loads the library until the
-// process exits).  Its device address comes from
+// How: the kernels' scratch (split-tile counters and fp32 partial tiles)
+// lives in the file-scope device array below (8 MiB, held by every GPU that
+// loads the library until the process exits); a call whose plan needs more
+// is refused.  Its device address comes from
 // cudaGetSymbolAddress, taken once per device with that device current, on
 // the first call on that device.  Each call then clears the counters with
 // cudaMemsetAsync on the caller's stream and runs the ordinary streaming path
@@ -36,14 +35,9 @@ void set_last_error(const char *msg);
 
 namespace {
 
-constexpr int kNoAllocMaxCtas = 160;
-constexpr int kNoAllocMaxK = 65536;
-// counters (rounded up to 256 bytes) + fp32 partial tiles, the layout of
-// stream_workspace_bytes(kNoAllocMaxCtas), then X as f16 for 16 tokens x
-// kNoAllocMaxK (tc_xbuf_bytes): 2,626,560 + 2,097,152 = 4,723,712 bytes
-constexpr size_t kNoAllocScratchBytes =
-    (((size_t)kNoAllocMaxCtas * kCountersPerCta * sizeof(unsigned) + 255) & ~(size_t)255) +
-    (size_t)kNoAllocMaxCtas * 2 * kConsumerWarps * kSlotFloats * sizeof(float) + (size_t)kNoAllocMaxK * 16 * 2;
+// counters + fp32 partial tiles: enough for 160 SMs with up to six row-block
+// segments per CTA (6 x 8 KiB partial tiles each) and 16384 row blocks.
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -76,22 +70,14 @@ extern "C" nvfp4_status nvfp4_gemv_batched_noalloc(const uint8_t *w_packed, cons
         return noalloc_fail(NVFP4_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices)
         return noalloc_fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_gemv_batched_noalloc: device ordinal too large");
-    int sms = 0;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-        return noalloc_fail(NVFP4_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
-    if (K > kNoAllocMaxK) {
-        char buf[160];
-        std::snprintf(buf, sizeof buf, "nvfp4_gemv_batched_noalloc: K = %d exceeds the static scratch's limit of %d",
-                      K, kNoAllocMaxK);
-        return noalloc_fail(NVFP4_ERR_WORKSPACE, buf);
-    }
-    const size_t needed = stream_workspace_bytes(sms) + tc_xbuf_bytes(K);
+    size_t counter_bytes = 0, needed = 0;
+    const int st = workspace_layout(n, N, K, nullptr, &counter_bytes, &needed);
+    if (st != NVFP4_OK) return (nvfp4_status)st;
     if (needed > kNoAllocScratchBytes) {
         char buf[256];
         std::snprintf(buf, sizeof buf,
-                      "nvfp4_gemv_batched_noalloc: this device has %d SMs and needs %zu bytes of scratch; the static "
-                      "scratch holds %zu bytes (up to %d SMs)",
-                      sms, needed, kNoAllocScratchBytes, kNoAllocMaxCtas);
+                      "nvfp4_gemv_batched_noalloc: this call needs %zu bytes of scratch; the static scratch holds %zu",
+                      needed, kNoAllocScratchBytes);
         return noalloc_fail(NVFP4_ERR_WORKSPACE, buf);
     }
     void *ptr = nullptr;
@@ -110,7 +96,7 @@ extern "C" nvfp4_status nvfp4_gemv_batched_noalloc(const uint8_t *w_packed, cons
     }
     // The split-tile counters must start at zero; the array keeps whatever the
     // last call left, so clear them on this stream before the kernels run.
-    if ((e = cudaMemsetAsync(ptr, 0, stream_counter_bytes(sms), stream)) != cudaSuccess)
+    if (counter_bytes && (e = cudaMemsetAsync(ptr, 0, counter_bytes, stream)) != cudaSuccess)
         return noalloc_fail(NVFP4_ERR_CUDA, std::string("cudaMemsetAsync(no-alloc counters): ") +
                                                 cudaGetErrorString(e));
     nvfp4_gemv_opts o;

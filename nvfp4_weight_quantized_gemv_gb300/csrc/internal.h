@@ -29,7 +29,6 @@ struct StreamParams {
     const uint16_t *x;   // [n][K] bf16, 16-byte aligned
     uint16_t *y;         // [n][N] bf16
     const float *gscale; // device scalar
-    const uint16_t *xf16;  // tcgen05 kernel: X converted to f16, [K/256][T][256] core-matrix slices
     float *partials;     // [C][2][kConsumerWarps][kSlotFloats]
     unsigned *counters;  // [C][kConsumerWarps]
     unsigned *err;       // device error word
@@ -54,18 +53,19 @@ inline int stream_smem_bytes(int stages, int n, int K) {
     return 1024 /* alignment slack */ + stages * kStageBytes + n * K * 2 + stages * 16 + 64;
 }
 
-// Workspace layout for a device with `max_ctas` SMs (independent of the grid
-// size of any one call, so counters always sit at the same place):
-//   [0, counter_bytes)          unsigned counters[max_ctas][kCountersPerCta]
-//   [counter_bytes, ...)        float partials[max_ctas][2][kConsumerWarps * kSlotFloats]
-inline size_t stream_counter_bytes(int max_ctas) {
-    return ((size_t)max_ctas * kCountersPerCta * sizeof(unsigned) + 255) & ~(size_t)255;
+// Workspace layout.  One zeroed counter region at offset 0 serves every
+// variant (each call leaves the counters it used at zero again):
+//   [0, counter_bytes)    unsigned counters: [sms][kCountersPerCta] for the
+//                         mma.sync / SIMT kernels, [row blocks][kConsumerWarps]
+//                         for the tcgen05 kernel
+//   [counter_bytes, ...)  float partial tiles of kConsumerWarps * kSlotFloats:
+//                         [sms][2] (mma.sync / SIMT) or [grid][max_seg] (tcgen05)
+//   then (tcgen05)        the f16 copy of X, tc_xbuf_bytes(K)
+inline size_t ws_counter_bytes(int sms, int row_blocks) {
+    const size_t a = (size_t)sms * kCountersPerCta, b = (size_t)row_blocks * kConsumerWarps;
+    return ((a > b ? a : b) * sizeof(unsigned) + 255) & ~(size_t)255;
 }
-inline size_t stream_workspace_bytes(int max_ctas) {
-    return stream_counter_bytes(max_ctas) + (size_t)max_ctas * 2 * kConsumerWarps * kSlotFloats * sizeof(float);
-}
-// The tcgen05 path also keeps X converted to f16 (16 tokens x K) after that.
-inline size_t tc_xbuf_bytes(int K) { return ((size_t)K * 16 * 2 + 255) & ~(size_t)255; }
+inline size_t stream_partial_bytes(int sms) { return (size_t)sms * 2 * kConsumerWarps * kSlotFloats * sizeof(float); }
 
 cudaError_t launch_stream(int variant, const CUtensorMap &tw, const CUtensorMap &ts, const StreamParams &p,
                           int smem, cudaStream_t stream);
@@ -73,14 +73,36 @@ cudaError_t launch_generic(const GenericParams &p, cudaStream_t stream);
 cudaError_t stream_set_smem_limits(int smem_optin);
 cudaError_t device_error_word(unsigned **ptr);  // device address of the error word
 
-// tcgen05 kernel (gemv_tc.cu): units of 128 rows x 256 k; T = 8 or 16 staged tokens.
+// tcgen05 kernel (gemv_tc.cu): units of 128 rows x 256 k; T = 8 or 16 staged
+// tokens; an even number of weight stages.  K is cut into `groups` k-groups
+// (tc_group_host: the first KC % groups get one unit column more); the CTAs
+// [cstart[g], cstart[g+1]) stream group g.  max_seg bounds the row blocks any
+// one CTA touches (its partial-tile slots).
 constexpr int kTcUnitKHost = 256;
-int tc_smem_bytes(int stages, int T, int K);
+constexpr int kTcMaxGroups = 32;
+struct TcPartition {
+    int groups;
+    int max_seg;
+    int row_blocks;
+    int cstart[kTcMaxGroups + 1];
+};
+int tc_smem_bytes(int stages, int T, int kg_max);
+void tc_group_host(int g, int groups, int KC, int *kstart, int *kg);
 cudaError_t tc_set_smem_limit(int smem_optin);
-// Converts X (n rows of bf16) into p.xf16 and then launches the GEMV with
-// programmatic dependent launch, so the GEMV's weight stream starts while X is
-// being converted.
-cudaError_t launch_tc(const CUtensorMap &tw, const CUtensorMap &ts, const StreamParams &p, int T, int smem,
-                      cudaStream_t stream);
+// Launches the GEMV with programmatic dependent launch: it may start (and
+// stream weights) while the kernel ahead of it on the stream is finishing; it
+// reads X and writes the workspace and Y only after that kernel completes.
+// tx: the f16 copy of X of this pass as a 3D tensor {64 k, n tokens, K/64},
+// box {64, T, 4} = one unit, 128-byte swizzle (tokens n..T-1 read as zeros).
+// Launches the X conversion (p.x -> xf, f16 x 2^-8, n rows) and then the
+// GEMV, both with programmatic dependent launch.
+cudaError_t launch_tc(const CUtensorMap &tw, const CUtensorMap &ts, const CUtensorMap &tx, const StreamParams &p,
+                      const TcPartition &part, int T, int smem, uint16_t *xf, cudaStream_t stream);
+// Bytes of the tcgen05 path's f16 copy of X (16 tokens x K).
+inline size_t tc_xbuf_bytes(int K) { return ((size_t)K * 16 * 2 + 255) & ~(size_t)255; }
+
+// Workspace a call needs (host-side plan; no GPU work): bytes of the zeroed
+// counter region at offset 0 and in total.  Returns an nvfp4_status.
+int workspace_layout(int n, int N, int K, const void *opts, size_t *counter_bytes, size_t *total_bytes);
 
 }  // namespace nvfp4

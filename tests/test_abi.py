@@ -59,6 +59,10 @@ def test_validation_errors_without_gpu():
     assert L.nvfp4_gemv_batched(None, None, None, None, None, 0, 128, 256, None) == nv.NVFP4_OK
     o = nv._opts(variant=7)
     assert L.nvfp4_gemv_batched_ex(p, p, p, p, p, 1, 128, 256, None, ctypes.byref(o)) == nv.NVFP4_ERR_INVALID_ARG
+    # the tcgen05 kernel takes an even number of weight stages
+    with pytest.raises(nv.Nvfp4Error, match="even"):
+        nv.nvfp4_gemv_plan(3, 4096, 4096, variant=nv.VARIANT_TC, stages=5)
+    assert nv.nvfp4_gemv_plan(3, 4096, 4096, variant=nv.VARIANT_MMA, stages=5)["stages"] == 5
     w = np.zeros((2, 24), dtype=np.float32)
     with pytest.raises(nv.Nvfp4Error):
         nv.nvfp4_quantize_ref(w)
@@ -81,7 +85,7 @@ def test_one_pass_plan():
         assert plan["units"] == (14336 // 128) * (5120 // 256)
         mma = nv.nvfp4_gemv_plan(n, 14336, 5120, variant=nv.VARIANT_MMA)
         assert mma["units"] == (14336 // 128) * (5120 // 128)
-        assert 2 <= plan["stages"] <= 8 and plan["smem_bytes"] <= 232448
+        assert 2 <= plan["stages"] <= 8 and plan["stages"] % 2 == 0 and plan["smem_bytes"] <= 232448
     # more than 16 tokens: chunks of 16
     assert nv.nvfp4_gemv_plan(20, 4096, 4096)["tile_tokens"] == [16, 4]
     # K too large for 16 tokens of X in shared memory: smaller chunks

@@ -114,13 +114,49 @@ def test_repeat_calls_are_bit_identical():
         assert np.array_equal(gpu_gemv(dev), first)
 
 
-@pytest.mark.parametrize("variant", ["tc", "mma"])
-@pytest.mark.parametrize("num_ctas,stages", [(1, 2), (3, 0), (7, 3), (0, 2), (150, 8)])
+@pytest.mark.parametrize("variant,num_ctas,stages", [
+    (v, c, s) for v in ("tc", "mma") for (c, s) in [(1, 2), (3, 0), (7, 4), (0, 2), (150, 8), (0, 6)]
+] + [("mma", 7, 3), ("mma", 5, 5)])
 def test_grid_and_ring_options(variant, num_ctas, stages):
     packed, scale, g, x = make_case(700, 1280, 4, 7, 8)
     y64, _ = oracle.gemv(packed, scale, g, x)
     y16 = gpu_gemv(to_gpu(packed, scale, g, x), VARIANTS[variant], num_ctas=num_ctas, stages=stages)
     assert_close(y16, y64)
+
+
+@pytest.mark.parametrize("N,K,n,num_ctas", [
+    (2000, 256, 4, 5),     # one unit per row block: every segment has one unit, two issuers idle
+    (1000, 512, 9, 3),     # segments of two units
+    (1000, 768, 16, 4),    # segments of three units, one per issuer
+    (3000, 1280, 2, 11),   # segments of five units, split row blocks
+])
+def test_short_segments(N, K, n, num_ctas):
+    """Row-block segments shorter than the issuer rotation (tcgen05 kernel)."""
+    packed, scale, g, x = make_case(N, K, n, 12, 13)
+    y64, _ = oracle.gemv(packed, scale, g, x)
+    assert_close(gpu_gemv(to_gpu(packed, scale, g, x), nv.VARIANT_TC, num_ctas=num_ctas), y64)
+
+
+def test_chained_calls_read_the_previous_output():
+    """Back-to-back calls on one stream where call 2 reads call 1's output as X:
+    the second kernel may start early (programmatic dependent launch) but must
+    read X and reuse the workspace only after the first has finished."""
+    p1, s1, g1, x = make_case(4096, 5120, 4, 20, 21)
+    p2, s2, g2, _ = make_case(2048, 4096, 1, 22, 23)
+    wp1, ws1, gs1, xt = to_gpu(p1, s1, g1, x)
+    wp2, ws2, gs2, _ = to_gpu(p2, s2, g2, x[:, :4096])
+    for _ in range(3):
+        y1 = nv.nvfp4_gemv_batched(wp1, ws1, gs1, xt)
+        y2 = nv.nvfp4_gemv_batched(wp2, ws2, gs2, y1)          # no synchronization in between
+        y3 = nv.nvfp4_gemv_batched(wp1, ws1, gs1, xt)
+        torch.cuda.synchronize()
+        y1h = y1.view(torch.int16).cpu().numpy().view(np.uint16)
+        y64, _ = oracle.gemv(p1, s1, g1, x)
+        assert_close(y1h, y64)
+        assert np.array_equal(y3.view(torch.int16).cpu().numpy(), y1.view(torch.int16).cpu().numpy())
+        y2_sync = nv.nvfp4_gemv_batched(wp2, ws2, gs2, y1)
+        torch.cuda.synchronize()
+        assert np.array_equal(y2.view(torch.int16).cpu().numpy(), y2_sync.view(torch.int16).cpu().numpy())
 
 
 def test_generic_paths_for_unaligned_or_ragged_k():
