@@ -11,10 +11,11 @@
 // stays resident in shared memory; the CTAs [cstart[g], cstart[g+1]) of the
 // persistent grid stream the units of group g in row-block-major order, each
 // CTA owning an equal contiguous range ("stream-K" within the group), so every
-// SM moves the same bytes.  A row block is finished by the last CTA to
-// complete its part of it, which sums the fp32 partial tiles of all its parts
-// in CTA order (fixed order: deterministic, and independent of n, since the
-// partition does not depend on n).
+// SM moves the same bytes.  A row block held whole by one CTA is finished
+// there; the parts of a split row block are published as fp32 tiles with
+// plain stores (no waiting inside the GEMV) and a small reduction kernel that
+// follows sums them in CTA order (fixed order: deterministic, and independent
+// of n, since the partition does not depend on n).
 //
 // X: a small kernel that runs first (xconvert_kernel) writes X as f16 times
 // 2^-8 (exact: a power of two) into the workspace, once per call; the GEMV
@@ -41,8 +42,9 @@
 //                and stores them with one tcgen05.st.  Each A buffer is
 //                handed over in two 128-k halves.
 //   warps 21-24  epilogue: per finished row-block segment, tcgen05.ld of the
-//                issuers' accumulators, summed in a fixed order, split
-//                fixup, x g x 2^8, bf16 store -- off the streaming path.
+//                issuers' accumulators, summed in a fixed order, then either
+//                x g x 2^8 and bf16 store (whole row block) or an fp32
+//                partial tile -- off the streaming path.
 //
 // With n <= 8 only tokens 0-7 are staged and the MMA's tokens 8-15 read a
 // 1024-byte zero block.  The 2^-8 prescale of X keeps |x| up to
@@ -87,7 +89,7 @@ constexpr int kTcThreads = (kTcWarpEpilogue0 + kTcEpilogueWarps) * 32;  // 800
 constexpr float kTcXScale = 1.0f / 256.0f;       // 2^-8 applied to X before the f16 cast
 constexpr float kTcXUnscale = 256.0f;
 constexpr unsigned kDevErrXRange = 8u;           // some |x| >= 65520 * 2^8
-constexpr int kTcPartialFloats = kConsumerWarps * kSlotFloats;  // one partial tile: 128 rows x 16 tokens
+constexpr int kTcPartialFloats = kConsumerWarps * kSlotFloats;  // one partial tile slot: 128 rows x 16 tokens
 
 static_assert(kTcDCol + kTcIssuers * 2 * 16 <= (int)kTcTmemCols, "tensor memory");
 
@@ -121,13 +123,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
         "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
         : "memory");
 }
-
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, bool &range) {
     const float lo = __uint_as_float(w << 16) * kTcXScale;
@@ -416,6 +411,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t lane_bits = (uint32_t)(32 * lq) << 16;
         griddep_wait();  // the global scale, the workspace and Y belong to this call from here on
         const float gs = __ldg(p.gscale) * kTcXUnscale;
+        (void)KC;
         int seg = 0, kl = kl0, rb = rb0;
         for (int i = 0; i < count; ++seg) {
             int iend = i + (kg - kl) - 1;
@@ -450,85 +446,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) mbar_arrive(sDEmpty + 8 * sb);
 
             const int row = rb * kUnitRows + 32 * lq + lane;
-            bool write = true;
-            if (!(G == 1 && kfirst == 0 && klast == kg - 1)) {
-                // Split row block: its parts are the ranges of CTAs cfirst..clast of every
-                // group.  The last CTA to finish its part sums all parts in CTA order.
-                unsigned parts = 0;
-                for (int g2 = 0; g2 < G; ++g2) {
-                    int ks2, kg2;
-                    tc_group(g2, G, KC, &ks2, &kg2);
-                    const int c2 = part.cstart[g2 + 1] - part.cstart[g2];
-                    const long long u2 = (long long)part.row_blocks * kg2;
-                    parts += (unsigned)(cta_of_unit_tc((long long)rb * kg2 + kg2 - 1, u2, c2) -
-                                        cta_of_unit_tc((long long)rb * kg2, u2, c2) + 1);
-                }
-                unsigned *const counter = &p.counters[(size_t)rb * kConsumerWarps + lq];
-                const int mine_slot = (int)blockIdx.x * part.max_seg + (rb - rb0);
-                // The CTA's last segment usually finishes after the other parts: check first,
-                // and skip publishing a partial nobody will read.
-                bool last = (iend == count - 1) && ld_acquire_gpu(counter) == parts - 1;
-                if (!last) {
-                    float4 *mine = reinterpret_cast<float4 *>(p.partials + (size_t)mine_slot * kTcPartialFloats +
-                                                              lq * 512 + lane * 16);
+            if (G == 1 && kfirst == 0 && klast == kg - 1) {
+                // the whole row block is this segment: finish it here
+                if (row < p.N) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) __stcg(mine + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
-                    fence_acq_rel_gpu();
-                    __syncwarp();
-                    unsigned old = 0;
-                    if (lane == 0) old = atomicAdd(counter, 1u);
-                    old = __shfl_sync(0xffffffffu, old, 0);
-                    last = old == parts - 1;
-                    if (last) fence_acq_rel_gpu();
-                }
-                write = last;
-                if (last) {
-                    float acc[16];
-                    bool any = false;
-                    for (int g2 = 0; g2 < G; ++g2) {
-                        int ks2, kg2;
-                        tc_group(g2, G, KC, &ks2, &kg2);
-                        const int cs2 = part.cstart[g2], c2 = part.cstart[g2 + 1] - cs2;
-                        const long long u2 = (long long)part.row_blocks * kg2;
-                        const int ca = cta_of_unit_tc((long long)rb * kg2, u2, c2);
-                        const int cb = cta_of_unit_tc((long long)rb * kg2 + kg2 - 1, u2, c2);
-                        for (int c = ca; c <= cb; ++c) {
-                            const int cta = cs2 + c;
-                            if (cta == (int)blockIdx.x) {
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) acc[j] = any ? acc[j] + v[j] : v[j];
-                                any = true;
-                                continue;
-                            }
-                            const int rbf = (int)(((long long)c * u2 / c2) / kg2);  // that CTA's first row block
-                            const float4 *src = reinterpret_cast<const float4 *>(
-                                p.partials + ((size_t)cta * part.max_seg + (rb - rbf)) * kTcPartialFloats + lq * 512 +
-                                lane * 16);
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const float4 f = __ldcg(src + q);
-                                if (!any) {
-                                    acc[4 * q] = f.x; acc[4 * q + 1] = f.y; acc[4 * q + 2] = f.z; acc[4 * q + 3] = f.w;
-                                } else {
-                                    acc[4 * q] += f.x; acc[4 * q + 1] += f.y; acc[4 * q + 2] += f.z; acc[4 * q + 3] += f.w;
-                                }
-                            }
-                            any = true;
+                    for (int t = 0; t < 16; ++t) {
+                        if (t < p.n) {
+                            __nv_bfloat16 hv = __float2bfloat16_rn(v[t] * gs);
+                            p.y[(size_t)t * p.N + row] = *reinterpret_cast<uint16_t *>(&hv);
                         }
                     }
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = acc[j];
-                    if (lane == 0) atomicExch(counter, 0u);
                 }
-            }
-            if (write && row < p.N) {
+            } else {
+                // one part of a split row block: publish the fp32 tile (T tokens per row);
+                // the reduction kernel that follows sums the parts in CTA order
+                float4 *mine = reinterpret_cast<float4 *>(
+                    p.partials + ((size_t)blockIdx.x * part.max_seg + (rb - rb0)) * kTcPartialFloats +
+                    (size_t)(32 * lq + lane) * T);
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    if (t < p.n) {
-                        __nv_bfloat16 hv = __float2bfloat16_rn(v[t] * gs);
-                        p.y[(size_t)t * p.N + row] = *reinterpret_cast<uint16_t *>(&hv);
-                    }
-                }
+                for (int q = 0; q < 4; ++q)
+                    if (q < T / 4) __stcg(mine + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
             }
             i = iend + 1;
             kl = 0;
@@ -541,6 +478,63 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == kTcWarpIssuer0) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tbase, kTcTmemCols);
+    }
+}
+
+// Split row blocks: one CTA per row block, one thread per row.  The parts of
+// row block rb are the unit ranges of CTAs [ca, cb] of every k-group, taken
+// in CTA order; part (CTA c) sits in c's slot for rb (c's partial tiles are
+// indexed by row block from its first one).  Row blocks finished whole by the
+// GEMV are skipped.
+__global__ void __launch_bounds__(kUnitRows) tc_reduce_kernel(const StreamParams p, const TcPartition part, const int T) {
+    griddep_launch_dependents();
+    griddep_wait();  // the GEMV's partial tiles are complete and visible
+    const int rb = blockIdx.x, G = part.groups, KC = p.KC;
+    const int r = threadIdx.x, row = rb * kUnitRows + r;
+    if (G == 1) {
+        int ks, kg;
+        tc_group(0, 1, KC, &ks, &kg);
+        const long long u = (long long)part.row_blocks * kg;
+        const int c0 = part.cstart[1];
+        if (cta_of_unit_tc((long long)rb * kg, u, c0) == cta_of_unit_tc((long long)rb * kg + kg - 1, u, c0)) return;
+    }
+    float acc[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) acc[t] = 0.f;
+    bool first = true;
+    for (int g = 0; g < G; ++g) {
+        int ks, kg;
+        tc_group(g, G, KC, &ks, &kg);
+        const int cs = part.cstart[g], cg = part.cstart[g + 1] - cs;
+        const long long u = (long long)part.row_blocks * kg;
+        const int ca = cta_of_unit_tc((long long)rb * kg, u, cg), cb = cta_of_unit_tc((long long)rb * kg + kg - 1, u, cg);
+        for (int c = ca; c <= cb; ++c) {
+            const int rbf = (int)(((long long)c * u / cg) / kg);  // that CTA's first row block
+            const float4 *src = reinterpret_cast<const float4 *>(
+                p.partials + ((size_t)(cs + c) * part.max_seg + (rb - rbf)) * kTcPartialFloats + (size_t)r * T);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (q < T / 4) {
+                    const float4 f = __ldcg(src + q);
+                    if (first) {
+                        acc[4 * q] = f.x; acc[4 * q + 1] = f.y; acc[4 * q + 2] = f.z; acc[4 * q + 3] = f.w;
+                    } else {
+                        acc[4 * q] += f.x; acc[4 * q + 1] += f.y; acc[4 * q + 2] += f.z; acc[4 * q + 3] += f.w;
+                    }
+                }
+            }
+            first = false;
+        }
+    }
+    if (row < p.N) {
+        const float gs = __ldg(p.gscale) * kTcXUnscale;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            if (t < p.n) {
+                __nv_bfloat16 hv = __float2bfloat16_rn(acc[t] * gs);
+                p.y[(size_t)t * p.N + row] = *reinterpret_cast<uint16_t *>(&hv);
+            }
+        }
     }
 }
 
@@ -571,7 +565,15 @@ cudaError_t launch_tc(const CUtensorMap &tw, const CUtensorMap &ts, const CUtens
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_tc_kernel, tw, ts, tx, p, part, T);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_tc_kernel, tw, ts, tx, p, part, T);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t rc = {};
+    rc.gridDim = dim3(part.row_blocks);
+    rc.blockDim = dim3(kUnitRows);
+    rc.stream = stream;
+    rc.attrs = attr;
+    rc.numAttrs = 1;
+    return cudaLaunchKernelEx(&rc, tc_reduce_kernel, p, part, T);
 }
 
 }  // namespace nvfp4
