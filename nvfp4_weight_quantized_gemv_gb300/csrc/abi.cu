@@ -239,6 +239,24 @@ static nvfp4_status tc_partition(int N, int K, int ctas, int smem_optin, TcParti
             if (segs > t.max_seg) t.max_seg = segs;
         }
     }
+    // parts of the most-split row block (the reduction kernel holds them all in shared memory)
+    if ((long long)t.row_blocks * KC * (ctas + 1) >= (1ll << 32))
+        return fail(NVFP4_ERR_UNSUPPORTED, "N = %d, K = %d: too many units for the tcgen05 kernel", N, K);
+    t.max_parts = 1;
+    for (int rb = 0; rb < t.row_blocks; ++rb) {
+        int parts = 0;
+        for (int g = 0; g < t.groups; ++g) {
+            int ks, kg;
+            tc_group_host(g, t.groups, KC, &ks, &kg);
+            const long long u = units[g];
+            const long long ca = ((long long)(rb * kg + 1) * c[g] - 1) / u, cb = ((long long)(rb * kg + kg) * c[g] - 1) / u;
+            parts += (int)(cb - ca + 1);
+        }
+        if (parts > t.max_parts) t.max_parts = parts;
+    }
+    if (t.max_parts > kTcMaxParts)
+        return fail(NVFP4_ERR_UNSUPPORTED, "a row block would be split into %d parts (at most %d)", t.max_parts,
+                    kTcMaxParts);
     *out = t;
     *kg_max_out = (KC + t.groups - 1) / t.groups;
     return NVFP4_OK;

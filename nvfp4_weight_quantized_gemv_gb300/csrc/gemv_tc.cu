@@ -484,47 +484,68 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // Split row blocks: one CTA per row block, one thread per row.  The parts of
 // row block rb are the unit ranges of CTAs [ca, cb] of every k-group, taken
 // in CTA order; part (CTA c) sits in c's slot for rb (c's partial tiles are
-// indexed by row block from its first one).  Row blocks finished whole by the
-// GEMV are skipped.
+// indexed by row block from its first one).  Each thread fetches its row of
+// kTcReduceChunk parts at a time into registers (all those loads in flight
+// together: one memory round trip per chunk), then sums them in order; no
+// shared memory, so the kernel never keeps the next GEMV off an SM.  Row
+// blocks finished whole by the GEMV (a single part) are skipped.  Index
+// arithmetic is 32-bit: the planner keeps row_blocks * KC * (grid + 1) below
+// 2^32.
 __global__ void __launch_bounds__(kUnitRows) tc_reduce_kernel(const StreamParams p, const TcPartition part, const int T) {
+    __shared__ int slots[kTcMaxParts];
+    __shared__ int nparts;
     griddep_launch_dependents();
-    griddep_wait();  // the GEMV's partial tiles are complete and visible
-    const int rb = blockIdx.x, G = part.groups, KC = p.KC;
-    const int r = threadIdx.x, row = rb * kUnitRows + r;
-    if (G == 1) {
-        int ks, kg;
-        tc_group(0, 1, KC, &ks, &kg);
-        const long long u = (long long)part.row_blocks * kg;
-        const int c0 = part.cstart[1];
-        if (cta_of_unit_tc((long long)rb * kg, u, c0) == cta_of_unit_tc((long long)rb * kg + kg - 1, u, c0)) return;
+    const unsigned rb = blockIdx.x;
+    const int G = part.groups, KC = p.KC;
+    if (threadIdx.x == 0) {
+        int np = 0;
+        for (int g = 0; g < G; ++g) {
+            int ks, kg;
+            tc_group(g, G, KC, &ks, &kg);
+            const unsigned cs = part.cstart[g], cg = part.cstart[g + 1] - cs;
+            const unsigned u = (unsigned)part.row_blocks * kg;
+            const unsigned ca = ((rb * kg + 1) * cg - 1) / u, cb = ((rb * kg + kg) * cg - 1) / u;
+            for (unsigned c = ca; c <= cb && np < kTcMaxParts; ++c) {
+                const unsigned rbf = (c * u / cg) / kg;  // that CTA's first row block
+                slots[np++] = (int)((cs + c) * part.max_seg + (rb - rbf));
+            }
+        }
+        nparts = np;
+    }
+    __syncthreads();
+    const int np = nparts;
+    if (np <= 1) return;  // finished whole by the GEMV
+    griddep_wait();       // the GEMV's partial tiles are complete and visible
+    const int r = threadIdx.x, row = (int)rb * kUnitRows + r;
+    const int nq = T / 4;  // float4 per row of a part
+    float4 a[4] = {};
+    for (int j0 = 0; j0 < np; j0 += kTcReduceChunk) {
+        float4 f[kTcReduceChunk][4];
+#pragma unroll
+        for (int j = 0; j < kTcReduceChunk; ++j) {
+            const float4 *src = reinterpret_cast<const float4 *>(
+                p.partials + (size_t)slots[j0 + j < np ? j0 + j : 0] * kTcPartialFloats + (size_t)r * T);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                f[j][q] = (j0 + j < np && q < nq) ? __ldcg(src + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < kTcReduceChunk; ++j) {
+            if (j0 + j >= np) break;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (j0 + j == 0) {
+                    a[q] = f[j][q];  // parts are summed in CTA order starting from the first
+                } else {
+                    a[q].x += f[j][q].x; a[q].y += f[j][q].y; a[q].z += f[j][q].z; a[q].w += f[j][q].w;
+                }
+            }
+        }
     }
     float acc[16];
 #pragma unroll
-    for (int t = 0; t < 16; ++t) acc[t] = 0.f;
-    bool first = true;
-    for (int g = 0; g < G; ++g) {
-        int ks, kg;
-        tc_group(g, G, KC, &ks, &kg);
-        const int cs = part.cstart[g], cg = part.cstart[g + 1] - cs;
-        const long long u = (long long)part.row_blocks * kg;
-        const int ca = cta_of_unit_tc((long long)rb * kg, u, cg), cb = cta_of_unit_tc((long long)rb * kg + kg - 1, u, cg);
-        for (int c = ca; c <= cb; ++c) {
-            const int rbf = (int)(((long long)c * u / cg) / kg);  // that CTA's first row block
-            const float4 *src = reinterpret_cast<const float4 *>(
-                p.partials + ((size_t)(cs + c) * part.max_seg + (rb - rbf)) * kTcPartialFloats + (size_t)r * T);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (q < T / 4) {
-                    const float4 f = __ldcg(src + q);
-                    if (first) {
-                        acc[4 * q] = f.x; acc[4 * q + 1] = f.y; acc[4 * q + 2] = f.z; acc[4 * q + 3] = f.w;
-                    } else {
-                        acc[4 * q] += f.x; acc[4 * q + 1] += f.y; acc[4 * q + 2] += f.z; acc[4 * q + 3] += f.w;
-                    }
-                }
-            }
-            first = false;
-        }
+    for (int q = 0; q < 4; ++q) {
+        acc[4 * q] = a[q].x; acc[4 * q + 1] = a[q].y; acc[4 * q + 2] = a[q].z; acc[4 * q + 3] = a[q].w;
     }
     if (row < p.N) {
         const float gs = __ldg(p.gscale) * kTcXUnscale;

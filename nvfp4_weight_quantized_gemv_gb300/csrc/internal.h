@@ -80,9 +80,12 @@ cudaError_t device_error_word(unsigned **ptr);  // device address of the error w
 // one CTA touches (its partial-tile slots).
 constexpr int kTcUnitKHost = 256;
 constexpr int kTcMaxGroups = 32;
+constexpr int kTcMaxParts = 256;   // most parts of one split row block
+constexpr int kTcReduceChunk = 4;  // partial tiles whose loads the reduction keeps in flight at once
 struct TcPartition {
     int groups;
     int max_seg;
+    int max_parts;
     int row_blocks;
     int cstart[kTcMaxGroups + 1];
 };
