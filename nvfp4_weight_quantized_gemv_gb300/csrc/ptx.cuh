@@ -57,15 +57,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, unsigned parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps (up to `ns` nanoseconds, or until the phase completes) instead of
+// spinning, so waiting warps leave the issue slots to the working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, unsigned parity, unsigned ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete, giving up after
-// kWaitLimitNs of wall-clock time.  Returns false on timeout (the caller sets
-// the error word and unwinds); never traps and never spins forever.
+// kWaitLimitNs of %globaltimer (returns false then).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, unsigned parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
-    for (unsigned it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 255u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
     }
 }
 

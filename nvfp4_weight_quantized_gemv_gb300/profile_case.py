@@ -30,7 +30,7 @@ def main():
     ap.add_argument("--shape", default="attn_qkv", choices=list(SHAPES))
     ap.add_argument("--ns", default="1,4")
     ap.add_argument("--reps", type=int, default=2)
-    ap.add_argument("--variant", default="auto", choices=["auto", "mma", "simt", "generic"])
+    ap.add_argument("--variant", default="auto", choices=["auto", "tc", "mma", "simt", "generic"])
     ap.add_argument("--tiling", default="one_pass", choices=["one_pass", "greedy_321"])
     args = ap.parse_args()
     nv.build()
@@ -39,7 +39,7 @@ def main():
     wp = torch.from_numpy(packed).cuda()
     ws = torch.from_numpy(scale).cuda()
     gs = torch.tensor([g], dtype=torch.float32, device="cuda")
-    variant = {"auto": 0, "mma": 1, "simt": 2, "generic": 3}[args.variant]
+    variant = {"auto": 0, "mma": 1, "simt": 2, "generic": 3, "tc": 4}[args.variant]
     tiling = nv.TILING_ONE_PASS if args.tiling == "one_pass" else nv.TILING_GREEDY_321
     for n in [int(v) for v in args.ns.split(",")]:
         x = torch.from_numpy(synth.activations_bf16(n, K, 1).view(np.int16)).cuda().view(torch.bfloat16)
