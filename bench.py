@@ -89,16 +89,22 @@ def kernel_traffic(variant):
     """Per-launch DRAM bytes of the variant's kernel from the committed ncu summary,
     if the kernel source is unchanged since those counters were taken."""
     src_name, prof_name, _ = KERNELS[variant]
-    src = os.path.join(ROOT, "nvfp4_weight_quantized_gemv_gb300", "csrc", src_name)
+    csrc = os.path.join(ROOT, "nvfp4_weight_quantized_gemv_gb300", "csrc")
     prof = os.path.join(ROOT, "profiles", prof_name)
     try:
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
         text = open(prof).read()
+        # every source hash the summary records must match the current file
+        checks = {"source_sha256": src_name, "ptx_sha256": "ptx.cuh", "tcgen05_sha256": "tcgen05.cuh"}
+        for key, name in checks.items():
+            m = re.search(key + r":\s*([0-9a-f]{64})", text)
+            if key == "source_sha256" and not m:
+                return None, None
+            if m and m.group(1) != hashlib.sha256(open(os.path.join(csrc, name), "rb").read()).hexdigest():
+                return None, None
     except OSError:
         return None, None
-    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     m_tr = re.search(r"dram_bytes_per_launch_n(\d+):\s*([0-9]+)", text)
-    if not m_sha or not m_tr or m_sha.group(1) != digest:
+    if not m_tr:
         return None, None
     return int(m_tr.group(2)), int(m_tr.group(1))
 
