@@ -205,11 +205,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // The weight stream starts first: the producer thread sets up the ring's
+    // barriers and requests the first stages before anything else (the ring is
+    // touched by no other thread before the CTA barrier below).
+    const uint64_t w_policy = l2_policy_evict_first();
+    int w_rb = rb0, w_kl = kl0, issued = 0;
+    auto issue_w = [&](int i) {
+        const int slot = i % S;
+        const uint32_t full = sFull + 8 * slot;
+        const int kc = kstart + w_kl;
+        mbar_arrive_expect_tx(full, kTcWBytes + kTcSBytes);
+        tma_load_2d(sW + slot * kTcWBytes, &tmap_w, kc * 128, w_rb * kUnitRows, full, w_policy);
+        tma_load_2d(sS + slot * kTcSBytes, &tmap_s, kc * 16, w_rb * kUnitRows, full, w_policy);
+        if (++w_kl == kg) {
+            w_kl = 0;
+            ++w_rb;
+        }
+    };
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(sFull + 8 * s, 1);
             mbar_init(sEmpty + 8 * s, kTcDequantWarps);
         }
+        fence_barrier_init();
+        for (; issued < (count < S ? count : S); ++issued) issue_w(issued);
         for (int s = 0; s < kg_max; ++s) mbar_init(sXFull + 8 * s, 1);
         for (int b = 0; b < 2 * kTcABufs; ++b) {
             mbar_init(sAFull + 8 * b, kTcDequantWarps / 2);
@@ -220,11 +239,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int h = 0; h < kTcIssuers; ++h) mbar_init(sFinal + 8 * h, 1);
         fence_barrier_init();
     }
-    if (warp == kTcWarpProducer && lane == 0) {
-        prefetch_tensormap(&tmap_w);
-        prefetch_tensormap(&tmap_s);
-        prefetch_tensormap(&tmap_x);
-    }
+    if (warp == kTcWarpX && lane == 0) prefetch_tensormap(&tmap_x);
     if (warp == kTcWarpIssuer0) {
         tc::tmem_alloc(sMisc, kTcTmemCols);
         tc::tmem_relinquish();
@@ -240,23 +255,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == kTcWarpProducer) {
         // ---------------------------------------------------------- TMA producer
         if (lane == 0) {
-            const uint64_t policy = l2_policy_evict_first();
-            int rb = rb0, kl = kl0;
-            auto issue_w = [&](int i) {
-                const int slot = i % S;
-                const uint32_t full = sFull + 8 * slot;
-                const int kc = kstart + kl;
-                mbar_arrive_expect_tx(full, kTcWBytes + kTcSBytes);
-                tma_load_2d(sW + slot * kTcWBytes, &tmap_w, kc * 128, rb * kUnitRows, full, policy);
-                tma_load_2d(sS + slot * kTcSBytes, &tmap_s, kc * 16, rb * kUnitRows, full, policy);
-                if (++kl == kg) {
-                    kl = 0;
-                    ++rb;
-                }
-            };
-            const int first = count < S ? count : S;
-            int issued = 0;
-            for (; issued < first; ++issued) issue_w(issued);
             for (; issued < count; ++issued) {
                 if (!mbar_wait_bounded(sEmpty + 8 * (issued % S), ((issued / S) - 1) & 1)) {
                     atomicOr(p.err, kDevErrTimeoutEmpty);
