@@ -46,11 +46,12 @@ extern "C" {
 typedef enum nvfp4_status {
     NVFP4_OK = 0,
     NVFP4_ERR_INVALID_ARG = 1,     /* null pointer, bad size, K % 16 != 0, ... */
-    NVFP4_ERR_MISALIGNED = 2,      /* reserved: unaligned inputs take a slower kernel instead */
+    NVFP4_ERR_MISALIGNED = 2,      /* device quantizer buffers unaligned (the GEMV takes a slower kernel instead) */
     NVFP4_ERR_UNSUPPORTED = 3,     /* device is not sm_103, or option not available */
     NVFP4_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed; see nvfp4_last_error() */
     NVFP4_ERR_DEVICE_TIMEOUT = 5,  /* a kernel gave up waiting on a barrier (see nvfp4_device_error) */
-    NVFP4_ERR_WORKSPACE = 6        /* caller workspace too small */
+    NVFP4_ERR_WORKSPACE = 6,       /* caller workspace too small */
+    NVFP4_ERR_DEVICE_INPUT = 7     /* a kernel met an input it cannot encode (see nvfp4_device_error) */
 } nvfp4_status;
 
 /* Kernel variants (selectable through nvfp4_gemv_opts; AUTO picks per shape). */
@@ -174,10 +175,44 @@ nvfp4_status nvfp4_gemv_plan(int n, int N, int K, const nvfp4_gemv_opts *opts,
 nvfp4_status nvfp4_quantize_ref(const float *w, int N, int K, uint8_t *w_packed, uint8_t *w_scale,
                                 float *global_scale);
 
-/* Synchronize `stream`, then report and clear the library's device error word.
- * *code receives the raw word (0 = no error).  Returns NVFP4_ERR_DEVICE_TIMEOUT
- * when a kernel gave up on a wait; the library then also re-zeroes its own
- * workspaces so later calls start clean. */
+/*
+ * Device NVFP4 quantizer: the runtime requantization of BF16 (or fp32)
+ * attention weights to FP4 that the pages' measurements depend on (atlas pull
+ * request #266, conversation, "Tiebreaker: the win is the BF16->FP4 requant
+ * path").  Same formula and fp32 rounding as nvfp4_quantize_ref (every
+ * division and product correctly rounded, no fused multiply-add), so for the
+ * same weights it writes the same bytes and the same g.  nvfp4_quantize_bf16
+ * takes bf16 weights (uint16 bit patterns), widened exactly to fp32 first.
+ *
+ * w_f32 / w_bf16: device [N][K], read only, 16-byte aligned.
+ * w_packed: device [N][K/2], written, 8-byte aligned (layout of the file header).
+ * w_scale_e4m3: device [N][K/16], written.
+ * w_global_scale_f32: device, 1 float, 4-byte aligned, written (it holds amax
+ *   between the launches, so it must not be read by other work until the call's
+ *   launches on `stream` are done).
+ * N >= 1, K >= 16, K % 16 == 0, N * K <= 2^40.  No output may overlap w.
+ * Three asynchronous launches on `stream` (amax reduction, block quantizer,
+ * finish) plus a 4-byte memset of w_global_scale_f32; no workspace.
+ * Errors: NVFP4_ERR_INVALID_ARG (null pointer, bad size), NVFP4_ERR_MISALIGNED
+ * (alignment above), NVFP4_ERR_CUDA.  A non-finite weight cannot be detected
+ * before launch: it sets bit 16 of the device error word (nvfp4_device_error
+ * then returns NVFP4_ERR_DEVICE_INPUT) and the outputs are not meaningful.
+ */
+nvfp4_status nvfp4_quantize(const float *w_f32, int N, int K, uint8_t *w_packed, uint8_t *w_scale_e4m3,
+                            float *w_global_scale_f32, cudaStream_t stream);
+nvfp4_status nvfp4_quantize_bf16(const uint16_t *w_bf16, int N, int K, uint8_t *w_packed,
+                                 uint8_t *w_scale_e4m3, float *w_global_scale_f32, cudaStream_t stream);
+
+/* Synchronize `stream`, then report and clear the library's device error word
+ * (one word per device, shared by every stream).  *code receives the raw word
+ * (0 = no error); its bits:
+ *   1, 2, 4  a GEMV kernel gave up on a wait (TMA stage full / stage free /
+ *            copies in flight at exit) after about 2 s;
+ *   8        the tcgen05 GEMV met |x| >= 65520 * 2^8 (see nvfp4_gemv_batched);
+ *   16       the device quantizer met a non-finite weight.
+ * Returns NVFP4_ERR_DEVICE_TIMEOUT when any of bits 1, 2, 4 is set (the
+ * library then also re-zeroes its own workspaces so later calls start clean),
+ * else NVFP4_ERR_DEVICE_INPUT when bit 8 or 16 is set, else NVFP4_OK. */
 nvfp4_status nvfp4_device_error(cudaStream_t stream, int *code);
 
 /* Message for the last non-OK status returned on this thread ("" if none). */

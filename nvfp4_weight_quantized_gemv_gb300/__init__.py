@@ -24,6 +24,7 @@ NVFP4_ERR_UNSUPPORTED = 3
 NVFP4_ERR_CUDA = 4
 NVFP4_ERR_DEVICE_TIMEOUT = 5
 NVFP4_ERR_WORKSPACE = 6
+NVFP4_ERR_DEVICE_INPUT = 7
 
 # nvfp4_variant / nvfp4_tiling
 VARIANT_AUTO, VARIANT_MMA, VARIANT_SIMT, VARIANT_GENERIC, VARIANT_TC = 0, 1, 2, 3, 4
@@ -34,7 +35,7 @@ TILING_NAMES = {0: "auto", 1: "one_pass", 2: "greedy_321"}
 # Names the C ABI exports (include/nvfp4_gemv.h).
 EXPORTS = ("nvfp4_gemv_batched", "nvfp4_gemv_batched_ex", "nvfp4_gemv_batched_noalloc",
            "nvfp4_gemv_workspace_size", "nvfp4_gemv_plan",
-           "nvfp4_quantize_ref", "nvfp4_device_error", "nvfp4_last_error", "nvfp4_version")
+           "nvfp4_quantize_ref", "nvfp4_quantize", "nvfp4_quantize_bf16", "nvfp4_device_error", "nvfp4_last_error", "nvfp4_version")
 
 
 class Nvfp4Error(RuntimeError):
@@ -81,6 +82,10 @@ def lib():
             L.nvfp4_gemv_plan.restype = i
             L.nvfp4_quantize_ref.argtypes = [vp, i, i, vp, vp, vp]
             L.nvfp4_quantize_ref.restype = i
+            L.nvfp4_quantize.argtypes = [vp, i, i, vp, vp, vp, vp]
+            L.nvfp4_quantize.restype = i
+            L.nvfp4_quantize_bf16.argtypes = [vp, i, i, vp, vp, vp, vp]
+            L.nvfp4_quantize_bf16.restype = i
             L.nvfp4_device_error.argtypes = [vp, ctypes.POINTER(i)]
             L.nvfp4_device_error.restype = i
             L.nvfp4_last_error.argtypes = []
@@ -202,11 +207,48 @@ def nvfp4_quantize_ref(w):
     return packed, scale, float(g[0])
 
 
+def _quantize_into(w, packed, scale, g, stream=None):
+    import torch
+    if w.dim() != 2 or not w.is_cuda or not w.is_contiguous():
+        raise ValueError("w must be a contiguous 2-D CUDA tensor")
+    N, K = w.shape
+    if w.dtype == torch.float32:
+        fn = lib().nvfp4_quantize
+    elif w.dtype == torch.bfloat16:
+        fn = lib().nvfp4_quantize_bf16
+    else:
+        raise ValueError(f"w must be float32 or bfloat16, not {w.dtype}")
+    _check(fn(w.data_ptr(), N, K, packed.data_ptr(), scale.data_ptr(), g.data_ptr(), _stream_handle(stream)))
+
+
+def nvfp4_quantize(w, stream=None):
+    """Device quantizer: CUDA float32 or bfloat16 W[N, K] -> (packed uint8 [N, K/2],
+    scale uint8 [N, K/16], g float32 [1]), all on W's device, written asynchronously
+    on `stream`.  Dispatches to nvfp4_quantize / nvfp4_quantize_bf16 by dtype."""
+    import torch
+    N, K = w.shape
+    packed = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    scale = torch.empty((N, K // 16), dtype=torch.uint8, device=w.device)
+    g = torch.empty(1, dtype=torch.float32, device=w.device)
+    _quantize_into(w, packed, scale, g, stream)
+    return packed, scale, g
+
+
+def nvfp4_quantize_bf16(w, stream=None):
+    """nvfp4_quantize for a bfloat16 W only (raises for any other dtype)."""
+    import torch
+    if w.dtype != torch.bfloat16:
+        raise ValueError(f"nvfp4_quantize_bf16 takes bfloat16 weights, not {w.dtype}")
+    return nvfp4_quantize(w, stream)
+
+
 def nvfp4_device_error(stream=None) -> int:
-    """Synchronize, read and clear the device error word; raises Nvfp4Error on a device timeout."""
+    """Synchronize, read and clear the device error word.  Returns the word
+    (0 = none; bits 8 and 16 flag inputs a kernel could not encode) and raises
+    Nvfp4Error when a kernel gave up on a wait (bits 1, 2, 4)."""
     code = ctypes.c_int(0)
     st = lib().nvfp4_device_error(_stream_handle(stream), ctypes.byref(code))
-    if st != NVFP4_OK and st != NVFP4_ERR_DEVICE_TIMEOUT:
+    if st not in (NVFP4_OK, NVFP4_ERR_DEVICE_TIMEOUT, NVFP4_ERR_DEVICE_INPUT):
         _check(st)
     if st == NVFP4_ERR_DEVICE_TIMEOUT:
         raise Nvfp4Error(st, nvfp4_last_error())

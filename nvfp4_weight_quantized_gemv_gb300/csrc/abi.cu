@@ -536,6 +536,42 @@ extern "C" nvfp4_status nvfp4_gemv_plan(int n, int N, int K, const nvfp4_gemv_op
     return NVFP4_OK;
 }
 
+// GPU quantizer entry points: validation as nvfp4_quantize_ref, plus device
+// pointer alignment (16 B for the weights, 8 B for the packed codes).
+template <typename TW>
+static nvfp4_status quantize_gpu(const TW *w, int N, int K, uint8_t *w_packed, uint8_t *w_scale,
+                                 float *w_global_scale, cudaStream_t stream, bool bf16) {
+    if (!w || !w_packed || !w_scale || !w_global_scale) return fail(NVFP4_ERR_INVALID_ARG, "null pointer argument");
+    if (N < 1) return fail(NVFP4_ERR_INVALID_ARG, "N = %d must be >= 1", N);
+    if (K < 16 || K % 16 != 0) return fail(NVFP4_ERR_INVALID_ARG, "K = %d must be a positive multiple of 16", K);
+    if ((long long)N * K > (1ll << 40)) return fail(NVFP4_ERR_INVALID_ARG, "N * K too large");
+    if (!aligned16(w) || (reinterpret_cast<uintptr_t>(w_packed) & 7u) != 0 ||
+        (reinterpret_cast<uintptr_t>(w_global_scale) & 3u) != 0)
+        return fail(NVFP4_ERR_MISALIGNED, "weights must be 16-byte aligned, packed codes 8-byte aligned");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    DeviceState *d = nullptr;
+    nvfp4_status st = device_state(dev, &d);
+    if (st != NVFP4_OK) return st;
+    e = bf16 ? launch_quantize_bf16(reinterpret_cast<const uint16_t *>(w), N, K, w_packed, w_scale, w_global_scale,
+                                    d->err_word, d->sms, stream)
+             : launch_quantize_f32(reinterpret_cast<const float *>(w), N, K, w_packed, w_scale, w_global_scale,
+                                   d->err_word, d->sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "quantizer launch");
+    return NVFP4_OK;
+}
+
+extern "C" nvfp4_status nvfp4_quantize(const float *w_f32, int N, int K, uint8_t *w_packed, uint8_t *w_scale_e4m3,
+                                       float *w_global_scale_f32, cudaStream_t stream) {
+    return quantize_gpu(w_f32, N, K, w_packed, w_scale_e4m3, w_global_scale_f32, stream, false);
+}
+
+extern "C" nvfp4_status nvfp4_quantize_bf16(const uint16_t *w_bf16, int N, int K, uint8_t *w_packed,
+                                            uint8_t *w_scale_e4m3, float *w_global_scale_f32, cudaStream_t stream) {
+    return quantize_gpu(w_bf16, N, K, w_packed, w_scale_e4m3, w_global_scale_f32, stream, true);
+}
+
 extern "C" nvfp4_status nvfp4_device_error(cudaStream_t stream, int *code) {
     if (!code) return fail(NVFP4_ERR_INVALID_ARG, "null code pointer");
     *code = 0;
@@ -553,6 +589,8 @@ extern "C" nvfp4_status nvfp4_device_error(cudaStream_t stream, int *code) {
     if (word == 0) return NVFP4_OK;
     const unsigned zero = 0;
     cudaMemcpy(d->err_word, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if ((word & 7u) == 0)
+        return fail(NVFP4_ERR_DEVICE_INPUT, "a kernel met an input it cannot encode (error word 0x%x)", word);
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         for (auto &w : g_workspaces)

@@ -67,6 +67,12 @@ inline size_t ws_counter_bytes(int sms, int row_blocks) {
 }
 inline size_t stream_partial_bytes(int sms) { return (size_t)sms * 2 * kConsumerWarps * kSlotFloats * sizeof(float); }
 
+// GPU quantizer (quantize_gpu.cu): three launches on `stream`; err = device error word.
+cudaError_t launch_quantize_f32(const float *w, int N, int K, uint8_t *packed, uint8_t *scale, float *global_scale,
+                                unsigned *err, int sms, cudaStream_t stream);
+cudaError_t launch_quantize_bf16(const uint16_t *w, int N, int K, uint8_t *packed, uint8_t *scale,
+                                 float *global_scale, unsigned *err, int sms, cudaStream_t stream);
+
 cudaError_t launch_stream(int variant, const CUtensorMap &tw, const CUtensorMap &ts, const StreamParams &p,
                           int smem, cudaStream_t stream);
 cudaError_t launch_generic(const GenericParams &p, cudaStream_t stream);

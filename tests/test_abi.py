@@ -68,6 +68,23 @@ def test_validation_errors_without_gpu():
         nv.nvfp4_quantize_ref(w)
 
 
+def test_device_quantizer_validation_without_gpu():
+    """nvfp4_quantize / nvfp4_quantize_bf16 reject bad arguments before any CUDA call."""
+    L = nv.lib()
+    a16, a8, a4 = ctypes.c_void_p(4096), ctypes.c_void_p(4096 + 8), ctypes.c_void_p(4096 + 4)
+    for fn in (L.nvfp4_quantize, L.nvfp4_quantize_bf16):
+        assert fn(None, 4, 64, a16, a16, a16, None) == nv.NVFP4_ERR_INVALID_ARG
+        assert fn(a16, 4, 64, a16, None, a16, None) == nv.NVFP4_ERR_INVALID_ARG
+        assert fn(a16, 0, 64, a16, a16, a16, None) == nv.NVFP4_ERR_INVALID_ARG
+        assert fn(a16, 4, 24, a16, a16, a16, None) == nv.NVFP4_ERR_INVALID_ARG
+        assert "multiple of 16" in nv.nvfp4_last_error()
+        assert fn(a16, 4, 0, a16, a16, a16, None) == nv.NVFP4_ERR_INVALID_ARG
+        assert fn(a16, 1 << 30, 1 << 14, a16, a16, a16, None) == nv.NVFP4_ERR_INVALID_ARG
+        assert fn(a8, 4, 64, a16, a16, a16, None) == nv.NVFP4_ERR_MISALIGNED      # weights need 16 B
+        assert fn(a16, 4, 64, a4, a16, a16, None) == nv.NVFP4_ERR_MISALIGNED      # codes need 8 B
+        assert fn(a16, 4, 64, a8, a16, ctypes.c_void_p(4098), None) == nv.NVFP4_ERR_MISALIGNED
+
+
 def test_greedy_321_tiling_matches_the_pages():
     # atlas #266 "What it does": greedy 3s then a 2-or-1 remainder; n = 8 -> 3 weight reads
     expect = {1: [1], 2: [2], 3: [3], 4: [3, 1], 5: [3, 2], 8: [3, 3, 2], 16: [3, 3, 3, 3, 3, 1]}
