@@ -110,11 +110,6 @@ __device__ __forceinline__ int cta_of_unit_tc(long long u, long long U, int C) {
     return (int)(((u + 1) * (long long)C - 1) / U);
 }
 
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int c0, int c1, int c2, uint32_t bar,
                                             uint64_t policy) {
     asm volatile(

@@ -115,6 +115,56 @@ def test_extreme_global_scales(amax):
     assert_same(w, gpu_quantize(w))
 
 
+def boundary_matrix(amax, bf16, seed):
+    """Weights placed on and a few ulps around every E2M1 decision point
+    T * d (T in 0.25, 0.75, ..., 5; d the block's fp32 divisor) for blocks
+    with a spread of scales, so each code decision is as close as the format
+    allows.  d and g are computed as the quantizer defines them (fp32 steps,
+    scale codes from the oracle's E4M3 encoder)."""
+    f32 = np.float32
+    rng = np.random.Generator(np.random.PCG64(seed))
+    N, K = 48, 16 * 32
+    w = np.zeros((N, K), dtype=f32)
+    g = f32(amax) / f32(2688.0)
+    thresholds = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    for r in range(N):
+        for b in range(K // 16):
+            B = f32(amax * 2.0 ** rng.uniform(-14, 0))
+            if bf16:
+                B = bf16_bits_to_f32(synth.to_bf16_bits(np.array([B], dtype=f32)))[0]
+            s_val = f32(oracle.e4m3_decode(oracle.e4m3_encode(float(B / (f32(6.0) * g)))))
+            d = s_val * g
+            vals = []
+            for t in thresholds:
+                x = np.float64(t) * np.float64(d)          # exact decision point
+                if bf16:
+                    u = int(synth.to_bf16_bits(np.array([x], dtype=f32))[0])
+                    vals += [bf16_bits_to_f32(np.array([u + k], dtype=np.uint16))[0] for k in (-1, 0, 1)]
+                else:
+                    c = f32(x)
+                    vals += [np.nextafter(c, f32(0)), c, np.nextafter(c, f32(np.inf))]
+            pick = rng.choice(len(vals), size=15, replace=False)
+            blk = np.array([vals[i] for i in pick], dtype=f32)
+            blk = np.where(blk < B, blk, f32(0.0))       # keep B the block maximum
+            signs = np.where(rng.random(15) < 0.5, f32(-1.0), f32(1.0))
+            w[r, b * 16:b * 16 + 15] = blk * signs
+            w[r, b * 16 + 15] = B
+    w[0, 15] = f32(amax)
+    return w
+
+
+@pytest.mark.parametrize("amax", [1.0, 0.7371, 313.25])
+def test_decision_boundaries_fp32(amax):
+    w = boundary_matrix(amax, bf16=False, seed=int(amax * 100))
+    assert_same(w, gpu_quantize(w))
+
+
+@pytest.mark.parametrize("amax", [1.0, 0.7371])
+def test_decision_boundaries_bf16(amax):
+    wb = synth.to_bf16_bits(boundary_matrix(amax, bf16=True, seed=int(amax * 100) + 1))
+    assert_same(bf16_bits_to_f32(wb), gpu_quantize(wb))
+
+
 def test_full_size_attention_qkv_bf16():
     """The attention qkv projection's shape (N = 14336, K = 5120), bf16 weights."""
     N, K = 14336, 5120
