@@ -332,8 +332,8 @@ def main():
         graphs.append(gph)
     plan = nv.nvfp4_gemv_plan(calls[-1][1], *SHAPES[calls[-1][0]], variant=variant, tiling=tiling)
     def launches(plan_info):
-        # tcgen05 path: X conversion, GEMV and split-row reduction per pass
-        return plan_info["passes"] * (3 if plan_info["variant"] == "tc" else 1)
+        # tcgen05 path: GEMV and split-row reduction per pass
+        return plan_info["passes"] * (2 if plan_info["variant"] == "tc" else 1)
 
     launches_per_step = sum(launches(nv.nvfp4_gemv_plan(n, *SHAPES[s], variant=variant, tiling=tiling))
                             for s, n in calls)

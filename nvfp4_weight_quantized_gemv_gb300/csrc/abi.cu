@@ -155,19 +155,21 @@ static nvfp4_status encode_2d(CUtensorMap *map, const void *ptr, uint64_t cols, 
     return NVFP4_OK;
 }
 
-// The f16 copy of X of one pass for the tcgen05 kernel, viewed as 3D {64 k,
-// n tokens, K/64 k-chunks} (token stride 2K bytes, chunk stride 128 bytes) so
-// that one box {64, T, 4} is one unit's X in the tensor core's
-// 128-byte-swizzled K-major layout; tokens past n read as zeros.
-static nvfp4_status encode_x(CUtensorMap *map, const uint16_t *x, int n, int K, int T) {
+// The bf16 X of one pass for the tcgen05 kernel with 16 staged tokens, viewed
+// as 3D {64 k, n tokens, K/64 k-chunks} (token stride 2K bytes, chunk stride
+// 128 bytes) so that one box {64, 16, 4} is one unit's X in the tensor core's
+// 128-byte-swizzled K-major layout; tokens past n read as zeros.  The kernel
+// converts the landed box to f16 in place.  (With 8 staged tokens the kernel
+// copies X rows itself and needs no map.)
+static nvfp4_status encode_x(CUtensorMap *map, const uint16_t *x, int n, int K) {
     EncodeTiledFn fn;
     nvfp4_status st = get_encode_fn(&fn);
     if (st != NVFP4_OK) return st;
     const cuuint64_t dims[3] = {64, (cuuint64_t)n, (cuuint64_t)K / 64};
     const cuuint64_t strides[2] = {(cuuint64_t)K * 2, 128};
-    const cuuint32_t box[3] = {64, (cuuint32_t)T, 4};
+    const cuuint32_t box[3] = {64, 16, 4};
     const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t *>(x), dims, strides, box, estr,
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(x), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled (X) failed (CUresult %d)", (int)r);
@@ -340,8 +342,7 @@ static nvfp4_status make_plan(int n, int N, int K, bool fast_ok, const nvfp4_gem
         p.tc_tokens = p.variant == kTc ? T : 0;
         p.counter_bytes = ws_counter_bytes(sms, (N + kUnitRows - 1) / kUnitRows);
         p.ws_bytes = p.counter_bytes + (p.variant == kTc ? (size_t)ctas * p.part.max_seg * kConsumerWarps *
-                                                                   kSlotFloats * sizeof(float) +
-                                                               tc_xbuf_bytes(K)
+                                                                   kSlotFloats * sizeof(float)
                                                          : stream_partial_bytes(sms));
     }
     *plan = p;
@@ -444,10 +445,10 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
         sp.n = tn;
         sp.y_vec2 = (N % 2 == 0) && ((reinterpret_cast<uintptr_t>(sp.y) & 3u) == 0);
         if (plan.variant == kTc) {
-            uint16_t *xf = reinterpret_cast<uint16_t *>(static_cast<char *>(work) + plan.ws_bytes - tc_xbuf_bytes(K));
             CUtensorMap tx;
-            if ((st = encode_x(&tx, xf, tn, K, plan.tc_tokens)) != NVFP4_OK) return st;
-            e = launch_tc(tw, ts, tx, sp, plan.part, plan.tc_tokens, plan.smem, xf, stream);
+            memset(&tx, 0, sizeof tx);
+            if (plan.tc_tokens == 16 && (st = encode_x(&tx, sp.x, tn, K)) != NVFP4_OK) return st;
+            e = launch_tc(tw, ts, tx, sp, plan.part, plan.tc_tokens, plan.smem, stream);
         } else {
             e = launch_stream(plan.variant, tw, ts, sp, plan.smem, stream);
         }

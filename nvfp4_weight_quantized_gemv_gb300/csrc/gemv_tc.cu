@@ -17,18 +17,20 @@
 // follows sums them in CTA order (fixed order: deterministic, and independent
 // of n, since the partition does not depend on n).
 //
-// X: a small kernel that runs first (xconvert_kernel) writes X as f16 times
-// 2^-8 (exact: a power of two) into the workspace, once per call; the GEMV
-// loads it from there.  Both are launched with programmatic dependent launch,
-// so each can start while the kernel ahead of it finishes.
+// X: each CTA stages the bf16 rows of its k-group's slice of X itself and
+// converts them to f16 times 2^-8 (exact: a power of two) in the tensor
+// core's K-major 128-byte-swizzled operand layout (8-token atoms of 1024 B).
+// With n <= 8 (T = 8) the X warp fetches each token's whole slice with one
+// bulk copy into a staging area, and the epilogue warps convert it into the
+// swizzled layout; rows n..7 are zeroed beforehand.  With T = 16 the X warp
+// loads one 3D TMA box per unit straight into the swizzled layout (rows
+// past n zero-filled) and the epilogue warps convert it in place.  No
+// separate conversion kernel or X buffer in global memory.
 //
 // Warp roles (800 threads, one CTA per SM):
 //   warp 0       weight producer: 2D TMA loads of the unit's W tile
 //                (128B-swizzled) and scale tile into a ring of S stages.
-//   warp 1       X: loads the group's slice of the f16 X once, one 3D TMA box
-//                per unit (64 k x T tokens x 4, 128-byte swizzled: the tensor
-//                core's K-major swizzled operand layout, 8-token atoms of
-//                1024 B), in the order the CTA uses them.
+//   warp 1       X loads (see above).
 //   warps 2-4    MMA issuers.  Unit i is multiplied by issuer i % 3 out of
 //                tensor-memory A buffer i % 3, so every barrier of a buffer
 //                has one waiter that sees each of its phases.  16 x
@@ -41,7 +43,9 @@
 //                unit into f16 (E2M1 cvt times the E4M3 block scale: exact)
 //                and stores them with one tcgen05.st.  Each A buffer is
 //                handed over in two 128-k halves.
-//   warps 21-24  epilogue: per finished row-block segment, tcgen05.ld of the
+//   warps 21-24  X conversion (bf16 -> f16 x 2^-8 in shared memory, unit by
+//                unit in the order the CTA uses them), then the epilogue:
+//                per finished row-block segment, tcgen05.ld of the
 //                issuers' accumulators, summed in a fixed order, then either
 //                x g x 2^8 and bf16 store (whole row block) or an fp32
 //                partial tile -- off the streaming path.
@@ -93,21 +97,17 @@ constexpr int kTcPartialFloats = kConsumerWarps * kSlotFloats;  // one partial t
 
 static_assert(kTcDCol + kTcIssuers * 2 * 16 <= (int)kTcTmemCols, "tensor memory");
 
-// barriers: full[S] empty[S] xfull[KG] afull[3][2] aempty[3][2] dfull[3][2] dempty[2] final[3]
+// barriers: full[S] empty[S] xloaded[KG] xfull[KG] afull[3][2] aempty[3][2] dfull[3][2] dempty[2] final[3]
 __host__ __device__ constexpr int tc_barrier_count(int S, int KG) {
-    return 2 * S + KG + 4 * kTcABufs + 2 * kTcIssuers + 2 + kTcIssuers;
+    return 2 * S + 2 * KG + 4 * kTcABufs + 2 * kTcIssuers + 2 + kTcIssuers;
 }
+constexpr int kTcXConverterWarps = kTcEpilogueWarps;  // the epilogue warps convert X before their epilogue work
 
 // Group g of `groups` k-groups over KC unit columns: first unit column and width.
 __host__ __device__ inline void tc_group(int g, int groups, int KC, int *kstart, int *kg) {
     const int q = KC / groups, r = KC % groups;
     *kg = q + (g < r ? 1 : 0);
     *kstart = g * q + (g < r ? g : r);
-}
-
-// CTA (local to its group) that owns unit u of a group with U units and C CTAs.
-__device__ __forceinline__ int cta_of_unit_tc(long long u, long long U, int C) {
-    return (int)(((u + 1) * (long long)C - 1) / U);
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int c0, int c1, int c2, uint32_t bar,
@@ -119,47 +119,49 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, bool &range) {
+// Plain bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// Two bf16 (one 32-bit word) -> two f16 of x * 2^-8.  `bad` collects, in
+// bits 15 and 31, finite entries with |x| >= 2^24: the only bf16 values whose
+// scaled f16 would overflow (65520 * 2^8 lies between 2^24 - 2^16 and 2^24).
+// Per 15-bit magnitude m: m + 0x3480 reaches bit 15 iff m >= 0x4B80 (2^24) and
+// m + 0x0080 iff m >= 0x7F80 (inf or NaN); neither sum carries out of its half.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, uint32_t &bad) {
+    const uint32_t m = w & 0x7FFF7FFFu;
+    bad |= (m + 0x34803480u) & ~(m + 0x00800080u) & 0x80008000u;
     const float lo = __uint_as_float(w << 16) * kTcXScale;
     const float hi = __uint_as_float(w & 0xFFFF0000u) * kTcXScale;
-    range |= (fabsf(lo) >= 65520.f && isfinite(lo)) || (fabsf(hi) >= 65520.f && isfinite(hi));
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// X[t][k] (bf16, t < n) -> xf[t][k] = f16(X * 2^-8), 8 k per thread.  Small
-// (few registers, no shared memory) so that it fits on an SM next to a
-// running GEMV CTA.  Every thread waits for the kernel ahead of it before
-// touching memory, so this grid never completes before that one.
-__global__ void __launch_bounds__(128) xconvert_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ xf,
-                                                       int n, int K, unsigned *err) {
-    griddep_launch_dependents();
-    griddep_wait();
-    const long long items = (long long)n * (K >> 3);
-    bool range = false;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < items;
-         i += (long long)gridDim.x * blockDim.x) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(x) + i);
-        const uint4 o = make_uint4(bf16x2_to_f16x2_scaled(v.x, range), bf16x2_to_f16x2_scaled(v.y, range),
-                                   bf16x2_to_f16x2_scaled(v.z, range), bf16x2_to_f16x2_scaled(v.w, range));
-        reinterpret_cast<uint4 *>(xf)[i] = o;
-    }
-    if (range) atomicOr(err, kDevErrXRange);
-}
-
 }  // namespace
 
+// X area: kg_max units x 16 token rows x 512 B -- the f16 X for T = 16, or
+// the f16 X (8 rows) plus the bf16 staging (8 rows) for T = 8: the same size,
+// so the plan does not depend on n.
 int tc_smem_bytes(int stages, int T, int kg_max) {
-    return 1024 + stages * (kTcWBytes + kTcSBytes) + kg_max * T * 512 + 1024 + 8 * tc_barrier_count(stages, kg_max) +
+    (void)T;
+    return 1024 + stages * (kTcWBytes + kTcSBytes) + kg_max * 16 * 512 + 1024 + 8 * tc_barrier_count(stages, kg_max) +
            64;
 }
 
 void tc_group_host(int g, int groups, int KC, int *kstart, int *kg) { tc_group(g, groups, KC, kstart, kg); }
 
+template <int T>  // staged tokens: 8 (n <= 8) or 16
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
-                   const __grid_constant__ CUtensorMap tmap_x, const StreamParams p, const TcPartition part,
-                   const int T) {
+                   const __grid_constant__ CUtensorMap tmap_x, const StreamParams p, const TcPartition part) {
+    static_assert(T == 8 || T == 16, "staged tokens");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t sW = (raw_addr + 1023u) & ~1023u;
@@ -182,14 +184,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int rb0 = (int)(u0 / kg), kl0 = (int)(u0 - (long long)rb0 * kg);  // first row block, column in group
     const int nx = count < kg ? count : kg;              // X units this CTA uses
 
-    const uint32_t xslot = (uint32_t)T * 512;           // one unit's X: 4 boxes of T tokens x 64 k (128 B rows)
-    const uint32_t xbox = (uint32_t)T * 128;
+    constexpr uint32_t xslot = (uint32_t)T * 512;       // one unit's X: 4 boxes of T tokens x 64 k (128 B rows)
+    constexpr uint32_t xbox = (uint32_t)T * 128;
     const uint32_t sS = sW + S * kTcWBytes;
     const uint32_t sX = sS + S * kTcSBytes;             // X of the group [kg_max units], 1024-byte aligned
-    const uint32_t sZero = sX + kg_max * xslot;         // 1024 zero bytes (one swizzle atom)
+    const uint32_t sStage = sX + kg_max * xslot;        // T = 8: bf16 rows [8 tokens][kg_max * 256 k]
+    const uint32_t stage_pitch = (uint32_t)kg_max * 512; // bytes per staged token row
+    const uint32_t sZero = sX + kg_max * 16 * 512;      // 1024 zero bytes (one swizzle atom)
     const uint32_t sFull = sZero + 1024;                // W + scales of a stage landed
     const uint32_t sEmpty = sFull + 8 * S;              // dequant warps done with W + scales, count 16
-    const uint32_t sXFull = sEmpty + 8 * S;             // [unit column] X landed (TMA), one phase
+    const uint32_t sXLoaded = sEmpty + 8 * S;           // [unit column] bf16 X landed (TMA), one phase
+    const uint32_t sXFull = sXLoaded + 8 * kg_max;      // [unit column] f16 X ready, count 5 (converter warps)
     const uint32_t sAFull = sXFull + 8 * kg_max;        // [buffer][half], count 8
     const uint32_t sAEmpty = sAFull + 16 * kTcABufs;    // [buffer][half], count 1 (commit)
     const uint32_t sDFull = sAEmpty + 16 * kTcABufs;    // [issuer][segment buffer], count 1 (commit)
@@ -224,7 +229,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         fence_barrier_init();
         for (; issued < (count < S ? count : S); ++issued) issue_w(issued);
-        for (int s = 0; s < kg_max; ++s) mbar_init(sXFull + 8 * s, 1);
+        for (int s = 0; s < kg_max; ++s) {
+            mbar_init(sXLoaded + 8 * s, 1);
+            mbar_init(sXFull + 8 * s, kTcXConverterWarps);
+        }
         for (int b = 0; b < 2 * kTcABufs; ++b) {
             mbar_init(sAFull + 8 * b, kTcDequantWarps / 2);
             mbar_init(sAEmpty + 8 * b, 1);
@@ -234,7 +242,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int h = 0; h < kTcIssuers; ++h) mbar_init(sFinal + 8 * h, 1);
         fence_barrier_init();
     }
-    if (warp == kTcWarpX && lane == 0) prefetch_tensormap(&tmap_x);
+    if (T == 16 && warp == kTcWarpX && lane == 0) prefetch_tensormap(&tmap_x);  // T = 8 uses no X map
     if (warp == kTcWarpIssuer0) {
         tc::tmem_alloc(sMisc, kTcTmemCols);
         tc::tmem_relinquish();
@@ -246,6 +254,71 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::fence_after_sync();
     const uint32_t tbase = misc[0];
     if (threadIdx.x == 0) griddep_launch_dependents();
+
+    // X conversion by the epilogue warps (converter cv = 0..3), unit column
+    // by unit column in the order the CTA uses them; each warp arrives on a
+    // column's barrier once its share of the column is stored.
+    //   T = 8:  rows t < n of column l come from the bf16 staging row of
+    //           token t (lane = 16-byte chunk of the column's 512 bytes) and
+    //           go to the chunk's swizzled position; rows n..7 are zeroed by
+    //           zero_x_pad before the wait for X.
+    //   T = 16: the landed TMA box is converted in place (rows past n are the
+    //           TMA's zero fill; a chunk's position inside the swizzled box
+    //           does not matter to an elementwise conversion).
+    auto zero_x_pad = [&](int cv) {
+        if (T != 8) return;
+        const int pad = T - p.n;
+        const int items = nx * 4 * pad * 8;  // 16-byte chunks
+        for (int j = cv * 32 + lane; j < items; j += kTcXConverterWarps * 32) {
+            const int c = j & 7, rowbox = j >> 3;  // rowbox = (column i * 4 + box b) * pad + (t - n)
+            const int tp = rowbox % pad, ib = rowbox / pad;
+            const int l = (kl0 + (ib >> 2)) % kg;
+            sts128(sX + l * xslot + (ib & 3) * xbox + (p.n + tp) * 128 + c * 16, make_uint4(0, 0, 0, 0));
+        }
+    };
+    auto convert_x = [&](int cv) -> bool {
+        uint32_t bad = 0;
+        bool ok = true;
+        if (T == 8 && __any_sync(0xffffffffu, !mbar_wait_bounded(sXLoaded, 0))) ok = false;
+        for (int i = 0; i < nx && ok && T == 8; ++i) {  // per column, so the MMAs can start early
+            const int l = (kl0 + i) % kg;
+            const uint32_t dst_box = sX + l * xslot + (uint32_t)(lane >> 3) * xbox;
+            for (int t = cv; t < p.n; t += kTcXConverterWarps) {
+                uint4 v = lds128(sStage + t * stage_pitch + l * 512 + lane * 16);
+                v.x = bf16x2_to_f16x2_scaled(v.x, bad);
+                v.y = bf16x2_to_f16x2_scaled(v.y, bad);
+                v.z = bf16x2_to_f16x2_scaled(v.z, bad);
+                v.w = bf16x2_to_f16x2_scaled(v.w, bad);
+                sts128(dst_box + t * 128 + ((uint32_t)((lane & 7) ^ (t & 7)) << 4), v);
+            }
+            fence_proxy_async_smem();  // the tensor core reads these bytes through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sXFull + 8 * l);
+        }
+        for (int i = 0; i < nx && ok && T == 16; ++i) {  // per column, as its box lands
+            const int l = (kl0 + i) % kg;
+            const uint32_t col = sX + l * xslot;
+            if (__any_sync(0xffffffffu, !mbar_wait_bounded(sXLoaded + 8 * l, 0))) {
+                ok = false;
+                break;
+            }
+            for (int c = cv * 32 + lane; c < 32 * T; c += kTcXConverterWarps * 32) {
+                if (((c >> 3) & (T - 1)) >= p.n) continue;  // row (c >> 3) = box * T + token
+                const uint32_t addr = col + (uint32_t)c * 16;
+                uint4 v = lds128(addr);
+                v.x = bf16x2_to_f16x2_scaled(v.x, bad);
+                v.y = bf16x2_to_f16x2_scaled(v.y, bad);
+                v.z = bf16x2_to_f16x2_scaled(v.z, bad);
+                v.w = bf16x2_to_f16x2_scaled(v.w, bad);
+                sts128(addr, v);
+            }
+            fence_proxy_async_smem();  // the tensor core reads these bytes through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sXFull + 8 * l);
+        }
+        if (bad) atomicOr(p.err, kDevErrXRange);
+        return ok;
+    };
 
     if (warp == kTcWarpProducer) {
         // ---------------------------------------------------------- TMA producer
@@ -270,18 +343,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp == kTcWarpX) {
         // ------------------------------------------------------------------- X
         // The unit in column l of the group sits at sX + l * xslot.
+        griddep_wait();  // X may be the output of the kernel ahead of this one
         if (lane == 0) {
-            griddep_wait();  // X is written by the conversion kernel that runs first
             const uint64_t policy = l2_policy_evict_last();  // every CTA of the group reads the same X
-            for (int i = 0; i < nx; ++i) {  // in the order the CTA uses them
-                const int l = (kl0 + i) % kg;
-                const uint32_t bar = sXFull + 8 * l;
-                mbar_arrive_expect_tx(bar, xslot);
-                tma_load_3d(sX + l * xslot, &tmap_x, 0, 0, (kstart + l) * 4, bar, policy);
+            if (T == 8) {
+                // one bulk copy per token: its kg units of the group, contiguous in X
+                const uint32_t bytes = (uint32_t)kg * 512;
+                mbar_arrive_expect_tx(sXLoaded, bytes * (uint32_t)p.n);
+                for (int t = 0; t < p.n; ++t)
+                    bulk_load(sStage + t * stage_pitch, p.x + (size_t)t * p.K + (size_t)kstart * kTcUnitK, bytes,
+                              sXLoaded, policy);
+            } else {
+                for (int i = 0; i < nx; ++i) {  // in the order the CTA uses them
+                    const int l = (kl0 + i) % kg;
+                    const uint32_t bar = sXLoaded + 8 * l;
+                    mbar_arrive_expect_tx(bar, xslot);
+                    tma_load_3d(sX + l * xslot, &tmap_x, 0, 0, (kstart + l) * 4, bar, policy);
+                }
             }
-            // wait (bounded) for every copy before exiting (the issuers may have given up)
-            for (int i = 0; i < nx; ++i) {
-                if (!mbar_wait_bounded(sXFull + 8 * ((kl0 + i) % kg), 0)) {
+            // wait (bounded) for every copy before the warp leaves (the conversion may give up)
+            const int waits = T == 8 ? 1 : nx;
+            for (int i = 0; i < waits; ++i) {
+                const uint32_t bar = T == 8 ? sXLoaded : sXLoaded + 8 * ((kl0 + i) % kg);
+                if (!mbar_wait_bounded(bar, 0)) {
                     atomicOr(p.err, kDevErrTimeoutDrain);
                     break;
                 }
@@ -318,6 +402,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const unsigned par = (ib / kTcABufs) & 1;
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
+                        // the two boxes (64 k each) of this half: tokens 8-15 are the next
+                        // atom (T == 16) or the zero block (T == 8)
+                        uint64_t bd[2];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t box = xbase + (uint32_t)(2 * half + h) * xbox;
+                            bd[h] = tc::smem_desc_sw128(box, (T == 16) ? 1024u : (sZero - box));
+                        }
                         if (!mbar_wait_bounded(sAFull + 8 * (a * 2 + half), par)) {
                             ok = false;
                             break;
@@ -325,11 +417,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tc::fence_after_sync();
 #pragma unroll
                         for (int s = 8 * half; s < 8 * half + 8; ++s) {
-                            // k-step s: box s/4, bytes 32*(s%4) into each 128-byte row; tokens
-                            // 8-15 are the next atom (T == 16) or the zero block (T == 8)
-                            const uint32_t box = xbase + (uint32_t)(s >> 2) * xbox;
-                            const uint64_t bdesc =
-                                tc::smem_desc_sw128(box + (uint32_t)(s & 3) * 32, (T == 16) ? 1024u : (sZero - box));
+                            // k-step s: box s/4, bytes 32*(s%4) into each 128-byte row (the
+                            // start-address field counts 16-byte units and does not carry)
+                            const uint64_t bdesc = bd[(s >> 2) & 1] + (uint64_t)(2 * (s & 3));
                             tc::mma_f16_ts(d_tmem, a_tmem + s * 8, bdesc, idesc, !(first && s == 0));
                         }
                         tc::commit(sAEmpty + 8 * (a * 2 + half));
@@ -355,26 +445,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int half = kq >> 1;
         const int r = 32 * lq + lane;          // row within the unit
         const uint32_t lane_bits = (uint32_t)(32 * lq) << 16;
+        // this lane's 64 k of row r in stage 0: two swizzled 16-byte chunks of
+        // the packed row, and 4 scale bytes (4-byte aligned)
+        const uint32_t w_off0 = r * 128 + (uint32_t)(((2 * kq) ^ (r & 7)) << 4);
+        const uint32_t w_off1 = r * 128 + (uint32_t)(((2 * kq + 1) ^ (r & 7)) << 4);
+        const uint8_t *const s_row = base + (sS - sW) + r * 16 + kq * 4;
         bool ok = true;
+        int slot = 0, ab = 0;            // ring stage, A buffer (i % S, i % kTcABufs kept incrementally)
+        uint32_t fpar = 0, apar = 1;     // parities to wait for: full[slot]; aempty[ab] from round 1 on
         for (int i = 0; i < count; ++i) {
-            const int slot = i % S;
-            if (__any_sync(0xffffffffu, !mbar_wait_bounded(sFull + 8 * slot, (i / S) & 1))) {
+            if (__any_sync(0xffffffffu, !mbar_wait_bounded(sFull + 8 * slot, fpar))) {
                 ok = false;
                 break;
             }
-            // 64 k of row r: 32 packed bytes in 2 swizzled 16-byte chunks, 4 scale bytes
-            const uint32_t wrow = sW + slot * kTcWBytes + r * 128;
-            const uint4 w0 = lds128(wrow + (uint32_t)(((2 * kq) ^ (r & 7)) << 4));
-            const uint4 w1 = lds128(wrow + (uint32_t)(((2 * kq + 1) ^ (r & 7)) << 4));
-            const uint32_t sv = *reinterpret_cast<const uint32_t *>(base + (sS - sW) + slot * kTcSBytes + r * 16 + kq * 4);
+            const uint32_t wst = sW + slot * kTcWBytes;
+            const uint4 w0 = lds128(wst + w_off0);
+            const uint4 w1 = lds128(wst + w_off1);
+            const uint32_t sv = *reinterpret_cast<const uint32_t *>(s_row + slot * kTcSBytes);
             __syncwarp();
             if (lane == 0) mbar_arrive(sEmpty + 8 * slot);  // the weight stage may be refilled
+            if (++slot == S) {
+                slot = 0;
+                fpar ^= 1u;
+            }
             const uint32_t s01 = e4m3x2_to_f16x2(sv), s23 = e4m3x2_to_f16x2(sv >> 16);
             const uint32_t sc[4] = {dup_lo(s01), dup_hi(s01), dup_lo(s23), dup_hi(s23)};
-            const int ab = i % kTcABufs;
             if (i >= kTcABufs &&
-                __any_sync(0xffffffffu,
-                           !mbar_wait_bounded(sAEmpty + 8 * (ab * 2 + half), ((i / kTcABufs) - 1) & 1))) {
+                __any_sync(0xffffffffu, !mbar_wait_bounded(sAEmpty + 8 * (ab * 2 + half), apar))) {
                 ok = false;
                 break;
             }
@@ -396,13 +493,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(sAFull + 8 * (ab * 2 + half));
+            if (++ab == kTcABufs) {  // next round R = i / 3 + 1 waits for the phase of round R - 1
+                ab = 0;
+                apar ^= 1u;
+            }
         }
         if (!ok && lane == 0) atomicOr(p.err, kDevErrTimeoutFull);
     } else {
         // ----------------------------------------------------------- epilogue
         const int lq = warp & 3;
         const uint32_t lane_bits = (uint32_t)(32 * lq) << 16;
-        griddep_wait();  // the global scale, the workspace and Y belong to this call from here on
+        zero_x_pad(warp - kTcWarpEpilogue0);
+        griddep_wait();  // X, the global scale, the workspace and Y belong to this call from here on
+        if (!convert_x(warp - kTcWarpEpilogue0) && lane == 0) atomicOr(p.err, kDevErrTimeoutFull);
         const float gs = __ldg(p.gscale) * kTcXUnscale;
         (void)KC;
         int seg = 0, kl = kl0, rb = rb0;
@@ -507,8 +610,11 @@ __global__ void __launch_bounds__(kUnitRows) tc_reduce_kernel(const StreamParams
     }
     __syncthreads();
     const int np = nparts;
+    // Every CTA waits for the GEMV, also those with nothing to sum: this grid
+    // must not complete before the GEMV does, since the next kernel on the
+    // stream (possibly the next call, reading Y) waits only for this one.
+    griddep_wait();
     if (np <= 1) return;  // finished whole by the GEMV
-    griddep_wait();       // the GEMV's partial tiles are complete and visible
     const int r = threadIdx.x, row = (int)rb * kUnitRows + r;
     const int nq = T / 4;  // float4 per row of a part
     float4 a[4] = {};
@@ -553,25 +659,16 @@ __global__ void __launch_bounds__(kUnitRows) tc_reduce_kernel(const StreamParams
 }
 
 cudaError_t tc_set_smem_limit(int smem_optin) {
-    return cudaFuncSetAttribute(gemv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+    cudaError_t e = cudaFuncSetAttribute(gemv_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gemv_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
 }
 
 cudaError_t launch_tc(const CUtensorMap &tw, const CUtensorMap &ts, const CUtensorMap &tx, const StreamParams &p,
-                      const TcPartition &part, int T, int smem, uint16_t *xf, cudaStream_t stream) {
+                      const TcPartition &part, int T, int smem, cudaStream_t stream) {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    {
-        const long long items = (long long)p.n * (p.K >> 3);
-        cudaLaunchConfig_t xc = {};
-        xc.gridDim = dim3((unsigned)((items + 127) / 128 < 1184 ? (items + 127) / 128 : 1184));
-        xc.blockDim = dim3(128);
-        xc.stream = stream;
-        xc.attrs = attr;
-        xc.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&xc, xconvert_kernel, p.x, xf, p.n, p.K, p.err);
-        if (e != cudaSuccess) return e;
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.ctas);
     cfg.blockDim = dim3(kTcThreads);
@@ -579,7 +676,8 @@ cudaError_t launch_tc(const CUtensorMap &tw, const CUtensorMap &ts, const CUtens
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_tc_kernel, tw, ts, tx, p, part, T);
+    cudaError_t e = T == 16 ? cudaLaunchKernelEx(&cfg, gemv_tc_kernel<16>, tw, ts, tx, p, part)
+                            : cudaLaunchKernelEx(&cfg, gemv_tc_kernel<8>, tw, ts, tx, p, part);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t rc = {};
     rc.gridDim = dim3(part.row_blocks);

@@ -60,7 +60,6 @@ inline int stream_smem_bytes(int stages, int n, int K) {
 //                         for the tcgen05 kernel
 //   [counter_bytes, ...)  float partial tiles of kConsumerWarps * kSlotFloats:
 //                         [sms][2] (mma.sync / SIMT) or [grid][max_seg] (tcgen05)
-//   then (tcgen05)        the f16 copy of X, tc_xbuf_bytes(K)
 inline size_t ws_counter_bytes(int sms, int row_blocks) {
     const size_t a = (size_t)sms * kCountersPerCta, b = (size_t)row_blocks * kConsumerWarps;
     return ((a > b ? a : b) * sizeof(unsigned) + 255) & ~(size_t)255;
@@ -101,14 +100,13 @@ cudaError_t tc_set_smem_limit(int smem_optin);
 // Launches the GEMV with programmatic dependent launch: it may start (and
 // stream weights) while the kernel ahead of it on the stream is finishing; it
 // reads X and writes the workspace and Y only after that kernel completes.
-// tx: the f16 copy of X of this pass as a 3D tensor {64 k, n tokens, K/64},
-// box {64, T, 4} = one unit, 128-byte swizzle (tokens n..T-1 read as zeros).
-// Launches the X conversion (p.x -> xf, f16 x 2^-8, n rows) and then the
-// GEMV, both with programmatic dependent launch.
+// tx (T = 16 only): the pass's bf16 X (p.x) as a 3D tensor {64 k, n tokens,
+// K/64}, box {64, 16, 4} = one unit, 128-byte swizzle (tokens past n read as
+// zeros).  With T = 8 the kernel bulk-copies X rows from p.x itself.
+// Launches the GEMV and then the split-row reduction, both with programmatic
+// dependent launch.
 cudaError_t launch_tc(const CUtensorMap &tw, const CUtensorMap &ts, const CUtensorMap &tx, const StreamParams &p,
-                      const TcPartition &part, int T, int smem, uint16_t *xf, cudaStream_t stream);
-// Bytes of the tcgen05 path's f16 copy of X (16 tokens x K).
-inline size_t tc_xbuf_bytes(int K) { return ((size_t)K * 16 * 2 + 255) & ~(size_t)255; }
+                      const TcPartition &part, int T, int smem, cudaStream_t stream);
 
 // Workspace a call needs (host-side plan; no GPU work): bytes of the zeroed
 // counter region at offset 0 and in total.  Returns an nvfp4_status.

@@ -159,6 +159,29 @@ def test_chained_calls_read_the_previous_output():
         assert np.array_equal(y2.view(torch.int16).cpu().numpy(), y2_sync.view(torch.int16).cpu().numpy())
 
 
+def test_chained_calls_with_every_row_block_whole():
+    """As above, with a first call whose partition gives every CTA exactly one
+    whole row block (N = 152 row blocks, K = one unit): nothing is left for
+    the reduction kernel, which must still not complete before the GEMV."""
+    N1, K1 = 152 * 128, 256
+    plan = nv.nvfp4_gemv_plan(2, N1, K1)
+    if plan["variant"] != "tc" or plan["num_ctas"] != 152:
+        pytest.skip("needs the tcgen05 path on a 152-SM part")
+    p1, s1, g1, x = make_case(N1, K1, 2, 30, 31)
+    p2, s2, g2, _ = make_case(256, N1, 2, 32, 33)
+    wp1, ws1, gs1, xt = to_gpu(p1, s1, g1, x)
+    wp2, ws2, gs2, _ = to_gpu(p2, s2, g2, synth.activations_bf16(2, N1, 34))
+    y1_ref, _ = oracle.gemv(p1, s1, g1, x)
+    for _ in range(5):
+        y1 = nv.nvfp4_gemv_batched(wp1, ws1, gs1, xt)
+        y2 = nv.nvfp4_gemv_batched(wp2, ws2, gs2, y1)          # no synchronization in between
+        torch.cuda.synchronize()
+        y1h = y1.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert_close(y1h, y1_ref)
+        y2_ref, _ = oracle.gemv(p2, s2, g2, y1h)
+        assert_close(y2.view(torch.int16).cpu().numpy().view(np.uint16), y2_ref)
+
+
 def test_generic_paths_for_unaligned_or_ragged_k():
     # K % 256 != 0 -> generic kernel
     packed, scale, g, x = make_case(300, 784, 3, 2, 3)
