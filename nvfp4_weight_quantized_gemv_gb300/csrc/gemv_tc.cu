@@ -56,7 +56,8 @@
 // word (the output is then not meaningful).
 //
 // Programmatic dependent launch: the kernel lets the next kernel on the stream
-// launch as soon as all its CTAs run, and it starts its own weight stream
+// (the split-row reduction) launch once all its CTAs have finished their
+// epilogue work, and it starts its own weight stream
 // before the kernel ahead of it has finished; X, the global scale, the
 // workspace and Y are touched only after griddepcontrol.wait.  Weights and
 // scales are therefore read as constants of the call.
@@ -97,10 +98,14 @@ constexpr int kTcPartialFloats = kConsumerWarps * kSlotFloats;  // one partial t
 
 static_assert(kTcDCol + kTcIssuers * 2 * 16 <= (int)kTcTmemCols, "tensor memory");
 
-// barriers: full[S] empty[S] xloaded[KG] xfull[KG] afull[3][2] aempty[3][2] dfull[3][2] dempty[2] final[3]
+// barriers: full[S] empty[S] xloaded[KG] xfull[KG] afull[3][2] aempty[3][2] dfull[3][2] dempty[2] final[3] xreq
 __host__ __device__ constexpr int tc_barrier_count(int S, int KG) {
-    return 2 * S + 2 * KG + 4 * kTcABufs + 2 * kTcIssuers + 2 + kTcIssuers;
+    return 2 * S + 2 * KG + 4 * kTcABufs + 2 * kTcIssuers + 2 + kTcIssuers + 1;
 }
+// Weight stages requested before X: the rest of the ring is requested only
+// once the X warp has requested X, so that X does not queue behind a full
+// ring of weight traffic from this SM.
+constexpr int kTcStagesBeforeX = 4;
 constexpr int kTcXConverterWarps = kTcEpilogueWarps;  // the epilogue warps convert X before their epilogue work
 
 // Group g of `groups` k-groups over KC unit columns: first unit column and width.
@@ -200,7 +205,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t sDFull = sAEmpty + 16 * kTcABufs;    // [issuer][segment buffer], count 1 (commit)
     const uint32_t sDEmpty = sDFull + 16 * kTcIssuers;  // [segment buffer], count 4 (epilogue warps)
     const uint32_t sFinal = sDEmpty + 16;               // [issuer], count 1 (commit)
-    const uint32_t sMisc = sFinal + 8 * kTcIssuers;     // [0] tensor-memory base
+    const uint32_t sXReq = sFinal + 8 * kTcIssuers;     // X requested (X warp), count 1
+    const uint32_t sMisc = sXReq + 8;                   // [0] tensor-memory base
     uint32_t *const misc = reinterpret_cast<uint32_t *>(base + (sMisc - sW));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -228,7 +234,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(sEmpty + 8 * s, kTcDequantWarps);
         }
         fence_barrier_init();
-        for (; issued < (count < S ? count : S); ++issued) issue_w(issued);
+        const int pre = count < kTcStagesBeforeX ? count : (kTcStagesBeforeX < S ? kTcStagesBeforeX : S);
+        for (; issued < pre; ++issued) issue_w(issued);
         for (int s = 0; s < kg_max; ++s) {
             mbar_init(sXLoaded + 8 * s, 1);
             mbar_init(sXFull + 8 * s, kTcXConverterWarps);
@@ -240,6 +247,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int d = 0; d < 2 * kTcIssuers; ++d) mbar_init(sDFull + 8 * d, 1);
         for (int d = 0; d < 2; ++d) mbar_init(sDEmpty + 8 * d, kTcEpilogueWarps);
         for (int h = 0; h < kTcIssuers; ++h) mbar_init(sFinal + 8 * h, 1);
+        mbar_init(sXReq, 1);
         fence_barrier_init();
     }
     if (T == 16 && warp == kTcWarpX && lane == 0) prefetch_tensormap(&tmap_x);  // T = 8 uses no X map
@@ -253,7 +261,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tbase = misc[0];
-    if (threadIdx.x == 0) griddep_launch_dependents();
 
     // X conversion by the epilogue warps (converter cv = 0..3), unit column
     // by unit column in the order the CTA uses them; each warp arrives on a
@@ -323,6 +330,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == kTcWarpProducer) {
         // ---------------------------------------------------------- TMA producer
         if (lane == 0) {
+            if (issued < count && !mbar_wait_bounded(sXReq, 0)) atomicOr(p.err, kDevErrTimeoutEmpty);
             for (; issued < count; ++issued) {
                 if (!mbar_wait_bounded(sEmpty + 8 * (issued % S), ((issued / S) - 1) & 1)) {
                     atomicOr(p.err, kDevErrTimeoutEmpty);
@@ -361,6 +369,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tma_load_3d(sX + l * xslot, &tmap_x, 0, 0, (kstart + l) * 4, bar, policy);
                 }
             }
+            mbar_arrive(sXReq);  // the producer may request the rest of the weight ring
             // wait (bounded) for every copy before the warp leaves (the conversion may give up)
             const int waits = T == 8 ? 1 : nx;
             for (int i = 0; i < waits; ++i) {
@@ -567,6 +576,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             kl = 0;
             ++rb;
         }
+        // The reduction kernel may launch once every CTA is here: launched
+        // earlier, its CTAs would sit on SMs (waiting for this grid) that the
+        // next call's GEMV CTAs need.
+        if (warp == kTcWarpEpilogue0 && lane == 0) griddep_launch_dependents();
     }
 
     tc::fence_before_sync();
