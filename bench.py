@@ -44,8 +44,10 @@ FALLBACK_HBM_GBS = 6800.0
 COPIES = 16
 
 # workload -> list of (shape name, n) calls per step
-SHAPES = {"attn_qkv": (14336, 5120), "o_proj": (5120, 6144), "fused_qkv": (16384, 5120)}
-OUTLIER = {"attn_qkv": 0.0, "o_proj": 0.01, "fused_qkv": 0.0}
+SHAPES = {"attn_qkv": (14336, 5120), "o_proj": (5120, 6144), "fused_qkv": (16384, 5120),
+          # dense SwiGLU verify FFN, hidden 5120, intermediate 17408: gate/up rows interleaved, then down
+          "ffn_gu": (2 * 17408, 5120), "ffn_down": (5120, 17408)}
+OUTLIER = {"attn_qkv": 0.0, "o_proj": 0.01, "fused_qkv": 0.0, "ffn_gu": 0.0, "ffn_down": 0.0}
 
 
 def workload_calls(name: str, n_sweep: int):
@@ -57,6 +59,8 @@ def workload_calls(name: str, n_sweep: int):
         return [("fused_qkv", 16)]
     if name == "decode_step":
         return [(s, n_sweep) for _ in range(16) for s in ("attn_qkv", "o_proj")]
+    if name == "ffn_verify":
+        return [("ffn_gu", n_sweep), ("ffn_down", n_sweep)]
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -216,8 +220,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="attn_qkv", choices=["attn_qkv", "o_proj", "fused_qkv", "decode_step"])
-    ap.add_argument("--n", type=int, default=8, help="tokens per call for --workload decode_step")
+    ap.add_argument("--workload", default="attn_qkv",
+                    choices=["attn_qkv", "o_proj", "fused_qkv", "decode_step", "ffn_verify"])
+    ap.add_argument("--n", type=int, default=8, help="tokens per call for --workload decode_step / ffn_verify")
     ap.add_argument("--tiling", default="one_pass", choices=["one_pass", "greedy_321"])
     ap.add_argument("--variant", default="auto", choices=["auto", "mma", "simt", "generic"])
     ap.add_argument("--cpu-rows", type=int, default=96, help="oracle sample rows per host core and call")
@@ -237,7 +242,10 @@ def main():
         "o_proj": "output projection N=5120 K=6144, n=8, activations with 1% x20 outliers",
         "fused_qkv": "fused projection N=16384 K=5120, n=16",
         "decode_step": f"decode step: 16 x (qkv N=14336 K=5120, o_proj N=5120 K=6144), n={args.n}",
+        "ffn_verify": f"dense SwiGLU verify FFN D=5120 F=17408 (gate/up GEMV with fused SwiGLU, then down), "
+                      f"n={args.n}",
     }[args.workload]
+    is_ffn = args.workload == "ffn_verify"
 
     # ---------------------------------------------------- reference arm
     if args.impl == "reference":
@@ -289,7 +297,7 @@ def main():
         packed, scale, g = nv.nvfp4_quantize_ref(synth.weights_f32(N, K, 100 + si))
         wp0 = torch.from_numpy(packed).to(dev)
         ws0 = torch.from_numpy(scale).to(dev)
-        ncopies = COPIES if args.workload != "decode_step" else 16
+        ncopies = 4 if is_ffn else COPIES  # ffn: 4 x 150 MB of weights, well above L2
         copies = []
         for c in range(ncopies):
             copies.append((torch.roll(wp0, shifts=c * 97, dims=0).contiguous(),
@@ -312,7 +320,17 @@ def main():
     # calls never reuse a copy within 16 calls of each other.
     counters = {s: 0 for s in shapes_used}
 
+    h_ffn = torch.empty((args.n, SHAPES["ffn_down"][1]), dtype=torch.bfloat16, device=dev) if is_ffn else None
+
+    def ffn_call(c, x, y, st):
+        nv.nvfp4_ffn_swiglu(weights["ffn_gu"][c], weights["ffn_down"][c], x, h=h_ffn, y=y, stream=st)
+
     def enqueue_step(st):
+        if is_ffn:
+            c = counters["ffn_gu"] % len(weights["ffn_gu"])
+            counters["ffn_gu"] += 1
+            ffn_call(c, xs[calls[0]], ys[calls[1]], st)
+            return
         for s, n in calls:
             wp, ws, gs = weights[s][counters[s] % len(weights[s])]
             counters[s] += 1
@@ -375,7 +393,25 @@ def main():
 
     # per-call breakdown (each call shape timed alone, back-to-back graph replays)
     per_call = {}
-    for s, n in dict.fromkeys(calls):
+    if is_ffn:  # the FFN is one library call: time it alone over its weight copies
+        n = args.n
+        g1 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g1, stream=stream):
+            for c in range(len(weights["ffn_gu"])):
+                ffn_call(c, xs[calls[0]], ys[calls[1]], stream)
+        reps = 200
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g1.replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                g1.replay()
+            b.record(stream)
+        b.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (reps * len(weights["ffn_gu"]))
+        per_call[f"ffn_n{n}"] = {"us_per_call": round(us, 3), "GB_s": round(step_bytes / (us * 1e-6) / 1e9, 1)}
+    for s, n in ([] if is_ffn else dict.fromkeys(calls)):
         key = f"{s}_n{n}"
         g1 = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g1, stream=stream):
@@ -438,10 +474,18 @@ def main():
     # end to end through the public API with host buffers: every step copies
     # the activations in from pinned host memory and the outputs back out
     e2e_steps = max(20, min(2000, args.steps // 20))
-    h2d = sum(xs_host[(s, n)].numel() * 2 for s, n in calls)
-    d2h = sum(ys_host[(s, n)].numel() * 2 for s, n in calls)
+    io_calls = [calls[0]] if is_ffn else calls   # ffn: x goes in, y comes out (h stays on the device)
+    h2d = sum(xs_host[(s, n)].numel() * 2 for s, n in io_calls)
+    d2h = sum(ys_host[(s, n)].numel() * 2 for s, n in ([calls[1]] if is_ffn else calls))
 
     def e2e_step():
+        if is_ffn:
+            c = counters["ffn_gu"] % len(weights["ffn_gu"])
+            counters["ffn_gu"] += 1
+            xs[calls[0]].copy_(xs_host[calls[0]], non_blocking=True)
+            ffn_call(c, xs[calls[0]], ys[calls[1]], stream)
+            ys_host[calls[1]].copy_(ys[calls[1]], non_blocking=True)
+            return
         for s, n in calls:
             wp, ws, gs = weights[s][counters[s] % len(weights[s])]
             counters[s] += 1
@@ -467,7 +511,7 @@ def main():
         e2e_ms = float(t.item())
     e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
 
-    traffic, traffic_n = kernel_traffic(plan["variant"])
+    traffic, traffic_n = kernel_traffic(plan["variant"]) if not is_ffn else (None, None)
     achieved = step_bytes / (ms_per_step * 1e-3) / 1e9  # per GPU: algorithmic bytes per launch / launch time
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
@@ -477,7 +521,8 @@ def main():
                 "kernel": KERNELS[plan["variant"]][2],
                 "algorithmic_bytes_per_step": step_bytes,
                 "traffic_note": (f"ncu dram read+write bytes per launch at n={traffic_n}" if traffic else
-                                 "null: no ncu counters for the current kernel source")}
+                                 "null: the recorded ncu counters cover the attention qkv shape only" if is_ffn
+                                 else "null: no ncu counters for the current kernel source")}
 
     if dist is not None:
         dist.barrier()

@@ -155,6 +155,47 @@ nvfp4_status nvfp4_gemv_batched_noalloc(const uint8_t *w_packed, const uint8_t *
                                         const float *w_global_scale_f32, const uint16_t *x_bf16,
                                         uint16_t *y_bf16, int n, int N, int K, cudaStream_t stream);
 
+/*
+ * Gate/up projection with the SwiGLU activation fused into its output, for
+ * the dense FFN of the K=m speculative-verify step that runs through batched
+ * GEMV (rustdoc of spark_model/layers/mod.rs, FfnComponent: "dense SwiGLU";
+ * can_forward_km / try_forward_km, "K=m (m=4..8) verify FFN via batched
+ * GEMV").  The SwiGLU form is the usual one; the pages name it without a
+ * formula:
+ *
+ *     h[t, f] = bf16( silu(G[t, f]) * U[t, f] ),   silu(a) = a / (1 + exp(-a)),
+ *
+ * with G and U the fp32 GEMV results (x g, not rounded to bf16 first) of the
+ * gate and up rows, and silu and the product in fp32.
+ *
+ * w_packed [2F][K/2], w_scale_e4m3 [2F][K/16]: the gate and up matrices with
+ * their rows interleaved -- row 2f is gate row f, row 2f+1 is up row f -- and
+ * one global scale for both (quantize the interleaved matrix as one tensor,
+ * e.g. with nvfp4_quantize_bf16).  x_bf16 [n][K]; h_bf16 [n][F] is written.
+ * Same conventions and errors as nvfp4_gemv_batched (same invariant: a batched
+ * call equals n single-token calls bit for bit); runs on the tcgen05 path
+ * only, so K % 256 != 0 or unaligned inputs give NVFP4_ERR_UNSUPPORTED.
+ * F >= 1.
+ */
+nvfp4_status nvfp4_gemv_swiglu(const uint8_t *w_packed, const uint8_t *w_scale_e4m3,
+                               const float *w_global_scale_f32, const uint16_t *x_bf16, uint16_t *h_bf16,
+                               int n, int F, int K, cudaStream_t stream);
+
+/*
+ * Dense SwiGLU FFN of n tokens (the verify FFN above): h = nvfp4_gemv_swiglu
+ * (W_gu, x), then y = W_down . h with nvfp4_gemv_batched -- two calls on
+ * `stream`, each reading its weights once for all n tokens.
+ * x_bf16 [n][D], h_bf16 [n][F] (device scratch owned by the caller, written),
+ * y_bf16 [n][D] (written); W_gu as in nvfp4_gemv_swiglu with K = D; W_down
+ * [D][F/2] packed, [D][F/16] scales.  D and F: positive multiples of 16 (256
+ * for the fast path of each call).  Errors as the two calls.
+ */
+nvfp4_status nvfp4_ffn_swiglu(const uint8_t *w_gu_packed, const uint8_t *w_gu_scale_e4m3,
+                              const float *w_gu_global_scale_f32, const uint8_t *w_down_packed,
+                              const uint8_t *w_down_scale_e4m3, const float *w_down_global_scale_f32,
+                              const uint16_t *x_bf16, uint16_t *h_bf16, uint16_t *y_bf16, int n, int D, int F,
+                              cudaStream_t stream);
+
 /* Bytes of device workspace a call with these options needs (opts may be NULL). */
 nvfp4_status nvfp4_gemv_workspace_size(int n, int N, int K, const nvfp4_gemv_opts *opts,
                                        size_t *bytes);

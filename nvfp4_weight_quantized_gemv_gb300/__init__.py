@@ -34,6 +34,7 @@ TILING_NAMES = {0: "auto", 1: "one_pass", 2: "greedy_321"}
 
 # Names the C ABI exports (include/nvfp4_gemv.h).
 EXPORTS = ("nvfp4_gemv_batched", "nvfp4_gemv_batched_ex", "nvfp4_gemv_batched_noalloc",
+           "nvfp4_gemv_swiglu", "nvfp4_ffn_swiglu",
            "nvfp4_gemv_workspace_size", "nvfp4_gemv_plan",
            "nvfp4_quantize_ref", "nvfp4_quantize", "nvfp4_quantize_bf16", "nvfp4_device_error", "nvfp4_last_error", "nvfp4_version")
 
@@ -75,6 +76,10 @@ def lib():
             L.nvfp4_gemv_batched_ex.restype = i
             L.nvfp4_gemv_batched_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
             L.nvfp4_gemv_batched_noalloc.restype = i
+            L.nvfp4_gemv_swiglu.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
+            L.nvfp4_gemv_swiglu.restype = i
+            L.nvfp4_ffn_swiglu.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, vp]
+            L.nvfp4_ffn_swiglu.restype = i
             L.nvfp4_gemv_workspace_size.argtypes = [i, i, i, ctypes.POINTER(nvfp4_gemv_opts), ctypes.POINTER(sz)]
             L.nvfp4_gemv_workspace_size.restype = i
             L.nvfp4_gemv_plan.argtypes = [i, i, i, ctypes.POINTER(nvfp4_gemv_opts),
@@ -150,6 +155,37 @@ def nvfp4_gemv_batched(w_packed, w_scale, w_global_scale, x, y=None, stream=None
     n, N, K = _gemv_args(w_packed, w_scale, w_global_scale, x, y)
     _check(lib().nvfp4_gemv_batched(w_packed.data_ptr(), w_scale.data_ptr(), w_global_scale.data_ptr(),
                                     x.data_ptr(), y.data_ptr(), n, N, K, _stream_handle(stream)))
+    return y
+
+
+def nvfp4_gemv_swiglu(w_packed, w_scale, w_global_scale, x, h=None, stream=None):
+    """h[n, F] = bf16(silu(gate) * up) with gate/up rows interleaved in W [2F, K] (see the C header)."""
+    import torch
+    F = w_packed.shape[0] // 2
+    n = x.shape[0] if x.dim() == 2 else 1
+    K = x.shape[-1]
+    if h is None:
+        h = torch.empty((n, F), dtype=torch.bfloat16, device=x.device)
+    _check(lib().nvfp4_gemv_swiglu(w_packed.data_ptr(), w_scale.data_ptr(), w_global_scale.data_ptr(), x.data_ptr(),
+                                   h.data_ptr(), n, F, K, _stream_handle(stream)))
+    return h
+
+
+def nvfp4_ffn_swiglu(w_gu, w_down, x, h=None, y=None, stream=None):
+    """Dense SwiGLU FFN: w_gu = (packed [2F, D/2], scale [2F, D/16], g [1]) with gate/up rows interleaved,
+    w_down = (packed [D, F/2], scale [D, F/16], g [1]); x [n, D] bf16.  Returns y [n, D]."""
+    import torch
+    gp, gsc, gg = w_gu
+    dp, dsc, dg = w_down
+    n, D = x.shape
+    F = gp.shape[0] // 2
+    if h is None:
+        h = torch.empty((n, F), dtype=torch.bfloat16, device=x.device)
+    if y is None:
+        y = torch.empty((n, D), dtype=torch.bfloat16, device=x.device)
+    _check(lib().nvfp4_ffn_swiglu(gp.data_ptr(), gsc.data_ptr(), gg.data_ptr(), dp.data_ptr(), dsc.data_ptr(),
+                                  dg.data_ptr(), x.data_ptr(), h.data_ptr(), y.data_ptr(), n, D, F,
+                                  _stream_handle(stream)))
     return y
 
 

@@ -377,8 +377,9 @@ static nvfp4_gemv_opts default_opts() {
     return o;
 }
 
+// swiglu: rows 2f, 2f+1 of W are gate_f, up_f; y receives h[n][N/2] (tcgen05 path only).
 static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, const uint16_t *x, uint16_t *y, int n,
-                        int N, int K, cudaStream_t stream, const nvfp4_gemv_opts *opts) {
+                        int N, int K, cudaStream_t stream, const nvfp4_gemv_opts *opts, bool swiglu = false) {
     nvfp4_status st = validate(wp, ws, gs, x, y, n, N, K);
     if (st != NVFP4_OK) return st;
     const nvfp4_gemv_opts o = opts ? *opts : default_opts();
@@ -393,6 +394,10 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
     Plan plan;
     if ((st = make_plan(n, N, K, fast_ok, o, d->sms, d->smem_optin, &plan)) != NVFP4_OK) return st;
 
+    if (swiglu && plan.variant != kTc)
+        return fail(NVFP4_ERR_UNSUPPORTED,
+                    "the fused SwiGLU runs on the tcgen05 path only (K %% 256 == 0, 16-byte aligned inputs, variant "
+                    "AUTO or TC)");
     if (plan.variant == kGeneric) {
         int t0 = 0;
         for (int tn : plan.tiles) {
@@ -438,10 +443,12 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
     sp.K = K;
     sp.KC = K / (plan.variant == kTc ? kTcUnitKHost : kUnitK);
     sp.stages = plan.stages;
+    sp.swiglu = swiglu ? 1 : 0;
+    const size_t y_stride = swiglu ? (size_t)N / 2 : (size_t)N;
     int t0 = 0;
     for (int tn : plan.tiles) {
         sp.x = x + (size_t)t0 * K;
-        sp.y = y + (size_t)t0 * N;
+        sp.y = y + (size_t)t0 * y_stride;
         sp.n = tn;
         sp.y_vec2 = (N % 2 == 0) && ((reinterpret_cast<uintptr_t>(sp.y) & 3u) == 0);
         if (plan.variant == kTc) {
@@ -473,6 +480,28 @@ extern "C" nvfp4_status nvfp4_gemv_batched_ex(const uint8_t *w_packed, const uin
                                               uint16_t *y_bf16, int n, int N, int K, cudaStream_t stream,
                                               const nvfp4_gemv_opts *opts) {
     return run(w_packed, w_scale_e4m3, w_global_scale_f32, x_bf16, y_bf16, n, N, K, stream, opts);
+}
+
+extern "C" nvfp4_status nvfp4_gemv_swiglu(const uint8_t *w_packed, const uint8_t *w_scale_e4m3,
+                                          const float *w_global_scale_f32, const uint16_t *x_bf16, uint16_t *h_bf16,
+                                          int n, int F, int K, cudaStream_t stream) {
+    if (F < 1 || F > (1 << 29)) return fail(NVFP4_ERR_INVALID_ARG, "F = %d must be in [1, 2^29]", F);
+    return run(w_packed, w_scale_e4m3, w_global_scale_f32, x_bf16, h_bf16, n, 2 * F, K, stream, nullptr, true);
+}
+
+extern "C" nvfp4_status nvfp4_ffn_swiglu(const uint8_t *w_gu_packed, const uint8_t *w_gu_scale_e4m3,
+                                         const float *w_gu_global_scale_f32, const uint8_t *w_down_packed,
+                                         const uint8_t *w_down_scale_e4m3, const float *w_down_global_scale_f32,
+                                         const uint16_t *x_bf16, uint16_t *h_bf16, uint16_t *y_bf16, int n, int D,
+                                         int F, cudaStream_t stream) {
+    if (!w_down_packed || !w_down_scale_e4m3 || !w_down_global_scale_f32 || !y_bf16)
+        return fail(NVFP4_ERR_INVALID_ARG, "null pointer argument");
+    if (D < 16 || D % 16 != 0 || F < 16 || F % 16 != 0)
+        return fail(NVFP4_ERR_INVALID_ARG, "D = %d and F = %d must be positive multiples of 16", D, F);
+    nvfp4_status st = nvfp4_gemv_swiglu(w_gu_packed, w_gu_scale_e4m3, w_gu_global_scale_f32, x_bf16, h_bf16, n, F,
+                                        D, stream);
+    if (st != NVFP4_OK) return st;
+    return run(w_down_packed, w_down_scale_e4m3, w_down_global_scale_f32, h_bf16, y_bf16, n, D, F, stream, nullptr);
 }
 
 // Host-only planning (no CUDA calls when the device state is unknown: SM count

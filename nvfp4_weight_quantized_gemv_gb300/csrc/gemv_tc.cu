@@ -135,6 +135,38 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
+// Output of one finished row `row` (this lane's) for all tokens: y = bf16(v *
+// gs), or, with p.swiglu, the gated form -- the rows 2f (gate) and 2f + 1 (up)
+// of a pair sit in lanes 2i and 2i + 1 of the calling warp, and the even lane
+// stores h[t][f] = bf16(silu(gate) * up), silu(a) = a / (1 + exp(-a)), in fp32.
+// Every lane of the warp must call it (the pair exchange is a shuffle).
+__device__ __forceinline__ void tc_store_row(const StreamParams &p, const float (&v)[16], int row, float gs) {
+    const int lane = threadIdx.x & 31;
+    if (!p.swiglu) {
+        if (row < p.N) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                if (t < p.n) {
+                    __nv_bfloat16 hv = __float2bfloat16_rn(v[t] * gs);
+                    p.y[(size_t)t * p.N + row] = *reinterpret_cast<uint16_t *>(&hv);
+                }
+            }
+        }
+        return;
+    }
+    const int F = p.N >> 1;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+        const float a = v[t] * gs;
+        const float up = __shfl_down_sync(0xffffffffu, a, 1);
+        if (t < p.n && (lane & 1) == 0 && row < p.N) {
+            const float h = a / (1.0f + expf(-a)) * up;
+            __nv_bfloat16 hv = __float2bfloat16_rn(h);
+            p.y[(size_t)t * F + (row >> 1)] = *reinterpret_cast<uint16_t *>(&hv);
+        }
+    }
+}
+
 // Two bf16 (one 32-bit word) -> two f16 of x * 2^-8.  `bad` collects, in
 // bits 15 and 31, finite entries with |x| >= 2^24: the only bf16 values whose
 // scaled f16 would overflow (65520 * 2^8 lies between 2^24 - 2^16 and 2^24).
@@ -552,16 +584,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
             const int row = rb * kUnitRows + 32 * lq + lane;
             if (G == 1 && kfirst == 0 && klast == kg - 1) {
-                // the whole row block is this segment: finish it here
-                if (row < p.N) {
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        if (t < p.n) {
-                            __nv_bfloat16 hv = __float2bfloat16_rn(v[t] * gs);
-                            p.y[(size_t)t * p.N + row] = *reinterpret_cast<uint16_t *>(&hv);
-                        }
-                    }
-                }
+                tc_store_row(p, v, row, gs);  // the whole row block is this segment: finish it here
             } else {
                 // one part of a split row block: publish the fp32 tile (T tokens per row);
                 // the reduction kernel that follows sums the parts in CTA order
@@ -659,16 +682,7 @@ __global__ void __launch_bounds__(kUnitRows) tc_reduce_kernel(const StreamParams
     for (int q = 0; q < 4; ++q) {
         acc[4 * q] = a[q].x; acc[4 * q + 1] = a[q].y; acc[4 * q + 2] = a[q].z; acc[4 * q + 3] = a[q].w;
     }
-    if (row < p.N) {
-        const float gs = __ldg(p.gscale) * kTcXUnscale;
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            if (t < p.n) {
-                __nv_bfloat16 hv = __float2bfloat16_rn(acc[t] * gs);
-                p.y[(size_t)t * p.N + row] = *reinterpret_cast<uint16_t *>(&hv);
-            }
-        }
-    }
+    tc_store_row(p, acc, row, __ldg(p.gscale) * kTcXUnscale);
 }
 
 cudaError_t tc_set_smem_limit(int smem_optin) {

@@ -37,6 +37,7 @@ struct StreamParams {
     int n, N, K, KC;     // KC = K / 128
     int stages;
     int y_vec2;          // bf16x2 stores allowed (N even and y 4-byte aligned)
+    int swiglu;          // tcgen05 only: rows 2f, 2f+1 are gate_f, up_f; y is h[n][N/2] = silu(gate) * up
 };
 
 struct GenericParams {

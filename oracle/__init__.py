@@ -13,6 +13,8 @@ Parity status of each function (pins are in ``tests/test_oracle.py``):
     bfloat16 conversions, exact rational rounding).
   - gemv / gemv_rows / gemv_points: pinned (hand-worked golden cases, brute
     force against a dense numpy float64 reconstruction, invariants).
+  - swiglu / gemv_swiglu: pinned (tabulated sigmoid values, the interleaved
+    layout against two separate projections, special cases).
   - quantize: pinned against its definition (hand-derived golden codes, an
     argmin-over-the-code-table restatement, round-trip bounds).  Agreement with
     any third-party NVFP4 quantizer is parity unpinned: the pages print no
@@ -74,6 +76,9 @@ def _load():
             lib.oracle_gemv_rows.argtypes = [u8p, u8p, ctypes.c_float, u16p, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, f64p, u16p]
             lib.oracle_gemv_points.restype = ctypes.c_int
+            lib.oracle_swiglu.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.c_int, ctypes.c_int,
+                                          ctypes.POINTER(ctypes.c_double), u16p]
+            lib.oracle_swiglu.restype = ctypes.c_int
             lib.oracle_gemv_points.argtypes = [u8p, u8p, ctypes.c_float, u16p, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, i32p, i32p, ctypes.c_int, f64p, u16p]
             _lib = lib
@@ -175,3 +180,25 @@ def gemv_points(packed, scale, g, x, tok, row):
     if rc != 0:
         raise ValueError(f"oracle_gemv_points failed with code {rc}")
     return y64, y16
+
+
+# ------------------------------------------------------------------- SwiGLU
+def swiglu(gu64):
+    """gu64: float64 [n, 2F] (gate/up interleaved columns) -> (h64 [n, F], h16 uint16 bf16 bits [n, F])."""
+    gu = np.ascontiguousarray(gu64, dtype=np.float64)
+    n, F2 = gu.shape
+    F = F2 // 2
+    h64 = np.zeros((n, F), dtype=np.float64)
+    h16 = np.zeros((n, F), dtype=np.uint16)
+    rc = _load().oracle_swiglu(_ptr(gu, ctypes.c_double), n, F, _ptr(h64, ctypes.c_double),
+                               _ptr(h16, ctypes.c_uint16))
+    if rc != 0:
+        raise ValueError(f"oracle_swiglu failed with code {rc}")
+    return h64, h16
+
+
+def gemv_swiglu(packed, scale, g, x):
+    """Gate/up projection (rows 2f = gate f, 2f+1 = up f) followed by SwiGLU: (h64, h16) [n, F]."""
+    y64, _ = gemv(packed, scale, g, x)
+    return swiglu(y64)
+

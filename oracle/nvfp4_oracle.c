@@ -306,3 +306,32 @@ int oracle_gemv_points(const uint8_t *packed, const uint8_t *scale, float global
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ SwiGLU */
+
+/* Dense SwiGLU activation of the verify FFN (rustdoc of spark_model/layers/
+ * mod.rs, FfnComponent: "dense SwiGLU"; the pages give no formula, this is
+ * the standard one):  h[t, f] = silu(G[t, f]) * U[t, f],  silu(a) = a / (1 +
+ * exp(-a)).  gu64 holds the unrounded projection results of rows laid out
+ * gate/up interleaved: column 2f of token t is G[t, f], column 2f+1 is
+ * U[t, f] ([n][2F]).  h64 (may be NULL) gets the fp64 value, h16 (may be NULL)
+ * its bf16 rounding (nearest even, straight from fp64).  Returns 0, or 1 on
+ * bad sizes. */
+int oracle_swiglu(const double *gu64, int n, int F, double *h64, uint16_t *h16)
+{
+    if (n < 0 || F < 1)
+        return 1;
+    for (int t = 0; t < n; ++t) {
+        for (int f = 0; f < F; ++f) {
+            double g = gu64[(long)t * 2 * F + 2 * f];
+            double u = gu64[(long)t * 2 * F + 2 * f + 1];
+            double h = g / (1.0 + exp(-g)) * u;
+            if (h64)
+                h64[(long)t * F + f] = h;
+            if (h16)
+                h16[(long)t * F + f] = oracle_bf16_encode(h);
+        }
+    }
+    return 0;
+}
+

@@ -339,3 +339,51 @@ def test_quantize_rejects_bad_input():
     bad[1, 3] = np.inf
     with pytest.raises(ValueError):
         oracle.quantize(bad)
+
+
+# ------------------------------------------------------------------ SwiGLU
+# Logistic sigmoid at a few points, from standard tables (sigma(a) = 1/(1+e^-a)).
+SIGMOID_TABLE = {1.0: 0.7310585786300049, -2.0: 0.11920292202211755, 3.0: 0.9525741268224334,
+                 -0.5: 0.3775406687981454, 0.0: 0.5}
+
+
+def test_swiglu_matches_tabulated_sigmoid():
+    gates = list(SIGMOID_TABLE)
+    ups = [2.0, -1.5, 0.25, 4.0, 7.0]
+    gu = np.array([[v for pair in zip(gates, ups) for v in pair]], dtype=np.float64)
+    h64, h16 = oracle.swiglu(gu)
+    for f, (a, u) in enumerate(zip(gates, ups)):
+        assert math.isclose(h64[0, f], a * SIGMOID_TABLE[a] * u, rel_tol=1e-15, abs_tol=1e-300)
+        assert h16[0, f] == oracle.bf16_encode(h64[0, f])
+
+
+def test_swiglu_special_cases():
+    gu = np.array([[0.0, 123.0, 5.0, 0.0, 40.0, 2.0, -40.0, 3.0, -745.0, 1.0]], dtype=np.float64)
+    h64, h16 = oracle.swiglu(gu)
+    assert h64[0, 0] == 0.0 and h64[0, 1] == 0.0          # gate 0 or up 0
+    assert math.isclose(h64[0, 2], 80.0, rel_tol=1e-15)    # sigma(40) = 1 - 4e-18
+    assert abs(h64[0, 3]) < 1e-15                          # sigma(-40) ~ 4.2e-18
+    assert h64[0, 4] == 0.0 or abs(h64[0, 4]) < 1e-300     # exp overflow side: -745 / inf
+    assert h16[0, 0] == 0 and h16[0, 4] in (0, 0x8000)
+    assert h16[0, 3] == oracle.bf16_encode(h64[0, 3])      # tiny, still a normal bf16
+
+
+def test_gemv_swiglu_interleaving_matches_two_projections():
+    """Rows 2f / 2f+1 of the joint matrix are gate f / up f: the joint call
+    equals the activation applied to two separate projections."""
+    rng = np.random.Generator(np.random.PCG64(11))
+    F, K, n = 24, 64, 3
+    wg = rng.standard_normal((F, K), dtype=np.float32)
+    wu = rng.standard_normal((F, K), dtype=np.float32) * np.float32(0.5)
+    w = np.empty((2 * F, K), dtype=np.float32)
+    w[0::2], w[1::2] = wg, wu
+    packed, scale, g = oracle.quantize(w)
+    x = synth.activations_bf16(n, K, seed=12)
+    h64, h16 = oracle.gemv_swiglu(packed, scale, g, x)
+    g64, _ = oracle.gemv(packed[0::2], scale[0::2], g, x)
+    u64, _ = oracle.gemv(packed[1::2], scale[1::2], g, x)
+    expect = g64 / (1.0 + np.exp(-g64)) * u64
+    assert np.allclose(h64, expect, rtol=1e-13, atol=1e-13)
+    # swapping the roles changes the result (silu is not symmetric)
+    swapped = u64 / (1.0 + np.exp(-u64)) * g64
+    assert not np.allclose(h64, swapped, rtol=1e-3, atol=1e-3)
