@@ -46,8 +46,12 @@ COPIES = 16
 # workload -> list of (shape name, n) calls per step
 SHAPES = {"attn_qkv": (14336, 5120), "o_proj": (5120, 6144), "fused_qkv": (16384, 5120),
           # dense SwiGLU verify FFN, hidden 5120, intermediate 17408: gate/up rows interleaved, then down
-          "ffn_gu": (2 * 17408, 5120), "ffn_down": (5120, 17408)}
-OUTLIER = {"attn_qkv": 0.0, "o_proj": 0.01, "fused_qkv": 0.0, "ffn_gu": 0.0, "ffn_down": 0.0}
+          "ffn_gu": (2 * 17408, 5120), "ffn_down": (5120, 17408),
+          # one routed expert of an MoE layer (hidden 2048, expert intermediate 768): gate/up, down
+          "moe_gu": (2 * 768, 2048), "moe_down": (2048, 768)}
+OUTLIER = {"attn_qkv": 0.0, "o_proj": 0.01, "fused_qkv": 0.0, "ffn_gu": 0.0, "ffn_down": 0.0, "moe_gu": 0.0,
+           "moe_down": 0.0}
+MOE_EXPERTS, MOE_TOPK = 128, 8
 
 
 def workload_calls(name: str, n_sweep: int):
@@ -61,6 +65,8 @@ def workload_calls(name: str, n_sweep: int):
         return [(s, n_sweep) for _ in range(16) for s in ("attn_qkv", "o_proj")]
     if name == "ffn_verify":
         return [("ffn_gu", n_sweep), ("ffn_down", n_sweep)]
+    if name == "moe_decode":  # for the CPU sample: one expert's gate/up and down per assignment
+        return [("moe_gu", 1), ("moe_down", 1)]
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -213,6 +219,157 @@ def cpu_oracle_sample(calls, rows_per_core: int, cores: int, steps: int = 1):
     return nbytes / wall / 1e9, wall, sample
 
 
+# ----------------------------------------------------------------- MoE decode
+def run_moe(args, torch, nv, rank, world, local_rank, wl_desc, cores):
+    """One MoE layer's expert FFN for n decode tokens: grouped gate/up with fused
+    SwiGLU over the routed assignments, then grouped down; each active expert is
+    read once per step.  `value` = GB/s of the active experts' weights + X."""
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.Stream()
+    E, k, n = MOE_EXPERTS, MOE_TOPK, args.n
+    (Ngu, D), (Dd, F) = SHAPES["moe_gu"], SHAPES["moe_down"]
+    # expert weights: one host draw per matrix kind, quantized by the library's
+    # host quantizer, E copies with rows rolled (distinct per expert)
+    def stack(N, K, seed):
+        packed, scale, g = nv.nvfp4_quantize_ref(synth.weights_f32(N, K, seed))
+        wp0, ws0 = torch.from_numpy(packed).to(dev), torch.from_numpy(scale).to(dev)
+        wp = torch.stack([torch.roll(wp0, shifts=e * 37, dims=0) for e in range(E)]).contiguous()
+        ws = torch.stack([torch.roll(ws0, shifts=e * 37, dims=0) for e in range(E)]).contiguous()
+        return wp, ws, torch.full((E,), g, dtype=torch.float32, device=dev)
+    gu, down = stack(Ngu, D, 300), stack(Dd, F, 301)
+    # R seeded routings (distinct experts per token, sorted by expert), rotated per step
+    R = 8
+    rng = np.random.Generator(np.random.PCG64(7))
+    routes, active = [], []
+    for _ in range(R):
+        choice = np.stack([rng.choice(E, size=k, replace=False) for _ in range(n)])  # [n][k]
+        pairs = sorted((int(e), t) for t in range(n) for e in choice[t])
+        off = np.zeros(E + 1, dtype=np.int32)
+        for e, _ in pairs:
+            off[e + 1] += 1
+        off = np.cumsum(off).astype(np.int32)
+        tok = np.array([t for _, t in pairs], dtype=np.int32)
+        routes.append((torch.from_numpy(off).to(dev), torch.from_numpy(tok).to(dev)))
+        active.append(int((np.diff(off) > 0).sum()))
+    A = n * k
+    ident = torch.arange(A, dtype=torch.int32, device=dev)
+    x_host = torch.from_numpy(synth.activations_bf16(n, D, 1).view(np.int16)).view(torch.bfloat16).pin_memory()
+    x = x_host.to(dev)
+    h = torch.empty((A, F), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((A, D), dtype=torch.bfloat16, device=dev)
+    y_host = torch.empty((A, D), dtype=torch.bfloat16).pin_memory()
+    exp_bytes = Ngu * D // 2 + Ngu * D // 16 + Dd * F // 2 + Dd * F // 16
+    step_bytes = [a * exp_bytes + 2 * n * D for a in active]  # active experts read once + X
+    mean_bytes = sum(step_bytes) / R
+
+    def step(i, st):
+        off, tok = routes[i % R]
+        nv.nvfp4_moe_gemv_grouped(gu[0], gu[1], gu[2], x, off, tok, y=h, swiglu=True, stream=st)
+        # down: h rows are already one per assignment, grouped by expert
+        nv.nvfp4_moe_gemv_grouped(down[0], down[1], down[2], h, off, ident, y=y, stream=st)
+
+    with torch.cuda.stream(stream):
+        step(0, stream)
+    stream.synchronize()
+    graphs = []
+    for i in range(R):
+        gph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gph, stream=stream):
+            step(i, stream)
+        graphs.append(gph)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % R].replay()
+    stream.synchronize()
+    if nv.nvfp4_device_error(stream) != 0:
+        raise SystemExit("device error during warm-up")
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[i % R].replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if nv.nvfp4_device_error(stream) != 0:
+        raise SystemExit("device error during the timed region")
+    ms_per_step = ms / args.steps
+    value = world * mean_bytes / (ms_per_step * 1e-3) / 1e9
+    # end to end: X in from pinned host memory, Y out, every step
+    e2e_steps = max(20, min(2000, args.steps // 10))
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            x.copy_(x_host, non_blocking=True); step(i, stream); y_host.copy_(y, non_blocking=True)
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(e2e_steps):
+            x.copy_(x_host, non_blocking=True)
+            step(i, stream)
+            y_host.copy_(y, non_blocking=True)
+        b.record(stream)
+    b.synchronize()
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+    hbm_peak, peak_kind = peaks()
+    achieved = mean_bytes / (ms_per_step * 1e-3) / 1e9
+    if dist is not None:
+        dist.barrier()
+        if rank != 0:
+            dist.destroy_process_group()
+            return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        gbs, wall, sample = cpu_oracle_sample(workload_calls("moe_decode", n), args.cpu_rows, cores)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16*f16+f32 (nvfp4 weights, bf16 activations)",
+        "data": "synthetic (seeded PCG64: expert W~N(0,0.02) quantized to NVFP4, X~N(0,1) bf16, random top-k routing)",
+        "config": {"workload": wl_desc, "experts": E, "top_k": k, "tokens": n, "assignments": A,
+                   "active_experts_mean": round(sum(active) / R, 2), "routings_rotated": R,
+                   "per_token_bytes_if_not_grouped": A * exp_bytes,
+                   "l2": "active expert weights per step above L2; routings rotated", "parallelism": f"replicas x{world}"},
+        "per_call": {f"moe_step_n{n}": {"us_per_call": round(ms_per_step * 1e3, 3), "GB_s": round(achieved, 1),
+                                        "frac_of_measured_hbm": round(achieved / hbm_peak, 4)}},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "kernel": "moe_gemv_kernel", "algorithmic_bytes_per_step": round(mean_bytes),
+                     "traffic_note": "null: no ncu counters recorded for this workload"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * mean_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 # ------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -221,8 +378,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="attn_qkv",
-                    choices=["attn_qkv", "o_proj", "fused_qkv", "decode_step", "ffn_verify"])
-    ap.add_argument("--n", type=int, default=8, help="tokens per call for --workload decode_step / ffn_verify")
+                    choices=["attn_qkv", "o_proj", "fused_qkv", "decode_step", "ffn_verify", "moe_decode"])
+    ap.add_argument("--n", type=int, default=8,
+                    help="tokens per call for --workload decode_step / ffn_verify / moe_decode")
     ap.add_argument("--tiling", default="one_pass", choices=["one_pass", "greedy_321"])
     ap.add_argument("--variant", default="auto", choices=["auto", "mma", "simt", "generic"])
     ap.add_argument("--cpu-rows", type=int, default=96, help="oracle sample rows per host core and call")
@@ -244,6 +402,8 @@ def main():
         "decode_step": f"decode step: 16 x (qkv N=14336 K=5120, o_proj N=5120 K=6144), n={args.n}",
         "ffn_verify": f"dense SwiGLU verify FFN D=5120 F=17408 (gate/up GEMV with fused SwiGLU, then down), "
                       f"n={args.n}",
+        "moe_decode": f"MoE decode, {MOE_EXPERTS} experts D=2048 F=768, top-{MOE_TOPK} of n={args.n} tokens: "
+                      f"grouped read-once gate/up (+SwiGLU) then down",
     }[args.workload]
     is_ffn = args.workload == "ffn_verify"
 
@@ -274,6 +434,8 @@ def main():
     import nvfp4_weight_quantized_gemv_gb300 as nv
 
     nv.build()
+    if args.workload == "moe_decode":
+        return run_moe(args, torch, nv, rank, world, local_rank, wl_desc, cores)
     dist = None
     if world > 1:
         import torch.distributed as dist_mod

@@ -51,7 +51,7 @@ typedef enum nvfp4_status {
     NVFP4_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed; see nvfp4_last_error() */
     NVFP4_ERR_DEVICE_TIMEOUT = 5,  /* a kernel gave up waiting on a barrier (see nvfp4_device_error) */
     NVFP4_ERR_WORKSPACE = 6,       /* caller workspace too small */
-    NVFP4_ERR_DEVICE_INPUT = 7     /* a kernel met an input it cannot encode (see nvfp4_device_error) */
+    NVFP4_ERR_DEVICE_INPUT = 7     /* a kernel met an input it cannot use (see nvfp4_device_error) */
 } nvfp4_status;
 
 /* Kernel variants (selectable through nvfp4_gemv_opts; AUTO picks per shape). */
@@ -196,6 +196,41 @@ nvfp4_status nvfp4_ffn_swiglu(const uint8_t *w_gu_packed, const uint8_t *w_gu_sc
                               const uint16_t *x_bf16, uint16_t *h_bf16, uint16_t *y_bf16, int n, int D, int F,
                               cudaStream_t stream);
 
+/*
+ * Grouped read-once GEMV over routed experts, for MoE decode (rustdoc of
+ * spark_model/layers/mod.rs, moe_grouped_decode_min_rows: the grouped arm
+ * "reads each routed expert ONCE instead of once per token", on tokens
+ * sorted by expert).  For every expert e and every assignment j in
+ * [expert_offsets[e], expert_offsets[e+1]):
+ *
+ *     Y[j, r] = bf16( g_e * sum_k X[sorted_token[j], k] * E2M1(W_e[r, k]) * E4M3(S_e[r, k/16]) )
+ *
+ * or, with swiglu = 1, H[j, f] = bf16(silu(Y'[j, 2f]) * Y'[j, 2f+1]) from the
+ * unrounded values Y' (rows interleaved gate/up as in nvfp4_gemv_swiglu).
+ * Each assignment's sum is computed in a fixed order that does not depend on
+ * the other tokens routed to the same expert.  The routing weights and the
+ * combine of a token's expert outputs are not part of this call.
+ *
+ * w_packed [E][N][K/2], w_scale_e4m3 [E][N][K/16]: device, 16-byte aligned;
+ * w_global_scale_f32 [E]: device; x_bf16 [n_tokens][K]: device, 16-byte
+ * aligned; expert_offsets [E+1] and sorted_token [A] (int32): device;
+ * y_bf16 [A][N] (swiglu: [A][N/2]): device, written, row j = assignment j.
+ * E >= 1, A >= 0 (0: no-op), n_tokens >= 1, N a positive multiple of 16,
+ * K a multiple of 32 in [32, 7168] whose 16 staged tokens (8 with swiglu) and
+ * 16 weight rows fit shared memory (K <= 5632 without swiglu).  Each CTA
+ * bulk-copies one contiguous block of an expert's rows, so each routed
+ * expert is read once whatever its token count.  Asynchronous on `stream`;
+ * one launch.  Errors: NVFP4_ERR_INVALID_ARG, NVFP4_ERR_MISALIGNED,
+ * NVFP4_ERR_UNSUPPORTED (K too large), NVFP4_ERR_CUDA.
+ * Offsets outside [0, A] or decreasing and token indices outside
+ * [0, n_tokens) are skipped by the kernel and set bit 32 of the device error
+ * word (nvfp4_device_error).
+ */
+nvfp4_status nvfp4_moe_gemv_grouped(const uint8_t *w_packed, const uint8_t *w_scale_e4m3,
+                                    const float *w_global_scale_f32, const uint16_t *x_bf16,
+                                    const int32_t *expert_offsets, const int32_t *sorted_token, uint16_t *y_bf16,
+                                    int E, int A, int n_tokens, int N, int K, int swiglu, cudaStream_t stream);
+
 /* Bytes of device workspace a call with these options needs (opts may be NULL). */
 nvfp4_status nvfp4_gemv_workspace_size(int n, int N, int K, const nvfp4_gemv_opts *opts,
                                        size_t *bytes);
@@ -249,11 +284,12 @@ nvfp4_status nvfp4_quantize_bf16(const uint16_t *w_bf16, int N, int K, uint8_t *
  * (0 = no error); its bits:
  *   1, 2, 4  a GEMV kernel gave up on a wait (TMA stage full / stage free /
  *            copies in flight at exit) after about 2 s;
- *   8        the tcgen05 GEMV met |x| >= 65520 * 2^8 (see nvfp4_gemv_batched);
- *   16       the device quantizer met a non-finite weight.
+ *   8        a GEMV met |x| >= 65520 * 2^8 (see nvfp4_gemv_batched);
+ *   16       the device quantizer met a non-finite weight;
+ *   32       the grouped expert GEMV met bad routing data.
  * Returns NVFP4_ERR_DEVICE_TIMEOUT when any of bits 1, 2, 4 is set (the
  * library then also re-zeroes its own workspaces so later calls start clean),
- * else NVFP4_ERR_DEVICE_INPUT when bit 8 or 16 is set, else NVFP4_OK. */
+ * else NVFP4_ERR_DEVICE_INPUT when bit 8, 16 or 32 is set, else NVFP4_OK. */
 nvfp4_status nvfp4_device_error(cudaStream_t stream, int *code);
 
 /* Message for the last non-OK status returned on this thread ("" if none). */

@@ -34,7 +34,7 @@ TILING_NAMES = {0: "auto", 1: "one_pass", 2: "greedy_321"}
 
 # Names the C ABI exports (include/nvfp4_gemv.h).
 EXPORTS = ("nvfp4_gemv_batched", "nvfp4_gemv_batched_ex", "nvfp4_gemv_batched_noalloc",
-           "nvfp4_gemv_swiglu", "nvfp4_ffn_swiglu",
+           "nvfp4_gemv_swiglu", "nvfp4_ffn_swiglu", "nvfp4_moe_gemv_grouped",
            "nvfp4_gemv_workspace_size", "nvfp4_gemv_plan",
            "nvfp4_quantize_ref", "nvfp4_quantize", "nvfp4_quantize_bf16", "nvfp4_device_error", "nvfp4_last_error", "nvfp4_version")
 
@@ -80,6 +80,8 @@ def lib():
             L.nvfp4_gemv_swiglu.restype = i
             L.nvfp4_ffn_swiglu.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, vp]
             L.nvfp4_ffn_swiglu.restype = i
+            L.nvfp4_moe_gemv_grouped.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+            L.nvfp4_moe_gemv_grouped.restype = i
             L.nvfp4_gemv_workspace_size.argtypes = [i, i, i, ctypes.POINTER(nvfp4_gemv_opts), ctypes.POINTER(sz)]
             L.nvfp4_gemv_workspace_size.restype = i
             L.nvfp4_gemv_plan.argtypes = [i, i, i, ctypes.POINTER(nvfp4_gemv_opts),
@@ -189,6 +191,25 @@ def nvfp4_ffn_swiglu(w_gu, w_down, x, h=None, y=None, stream=None):
     return y
 
 
+def nvfp4_moe_gemv_grouped(w_packed, w_scale, w_global_scale, x, expert_offsets, sorted_token, y=None,
+                           swiglu=False, stream=None):
+    """Grouped read-once GEMV over routed experts (see the C header).
+
+    w_packed uint8 [E, N, K/2], w_scale uint8 [E, N, K/16], w_global_scale float32 [E], x bf16 [n, K],
+    expert_offsets int32 [E+1], sorted_token int32 [A].  Returns y bf16 [A, N] (swiglu: [A, N/2])."""
+    import torch
+    E, N, half_k = w_packed.shape
+    K = 2 * half_k
+    A = sorted_token.numel()
+    if y is None:
+        y = torch.empty((A, N // 2 if swiglu else N), dtype=torch.bfloat16, device=x.device)
+    _check(lib().nvfp4_moe_gemv_grouped(w_packed.data_ptr(), w_scale.data_ptr(), w_global_scale.data_ptr(),
+                                        x.data_ptr(), expert_offsets.data_ptr(), sorted_token.data_ptr(),
+                                        y.data_ptr(), E, A, x.shape[0], N, K, int(bool(swiglu)),
+                                        _stream_handle(stream)))
+    return y
+
+
 def nvfp4_gemv_batched_ex(w_packed, w_scale, w_global_scale, x, y=None, stream=None, variant=0, tiling=0,
                           num_ctas=0, stages=0, workspace=None):
     """nvfp4_gemv_batched with explicit variant / tiling / grid / ring depth / workspace."""
@@ -280,7 +301,7 @@ def nvfp4_quantize_bf16(w, stream=None):
 
 def nvfp4_device_error(stream=None) -> int:
     """Synchronize, read and clear the device error word.  Returns the word
-    (0 = none; bits 8 and 16 flag inputs a kernel could not encode) and raises
+    (0 = none; bits 8, 16 and 32 flag inputs a kernel could not use) and raises
     Nvfp4Error when a kernel gave up on a wait (bits 1, 2, 4)."""
     code = ctypes.c_int(0)
     st = lib().nvfp4_device_error(_stream_handle(stream), ctypes.byref(code))

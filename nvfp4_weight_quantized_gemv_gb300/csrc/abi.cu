@@ -79,6 +79,8 @@ static nvfp4_status device_state(int dev, DeviceState **out) {
             return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
         if ((e = tc_set_smem_limit(d.smem_optin)) != cudaSuccess)
             return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory, tcgen05 kernel)");
+        if ((e = moe_set_smem_limit(d.smem_optin)) != cudaSuccess)
+            return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory, grouped expert kernel)");
         if ((e = device_error_word(&d.err_word)) != cudaSuccess)
             return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
         d.ready = true;
@@ -602,6 +604,56 @@ extern "C" nvfp4_status nvfp4_quantize_bf16(const uint16_t *w_bf16, int N, int K
     return quantize_gpu(w_bf16, N, K, w_packed, w_scale_e4m3, w_global_scale_f32, stream, true);
 }
 
+extern "C" nvfp4_status nvfp4_moe_gemv_grouped(const uint8_t *w_packed, const uint8_t *w_scale_e4m3,
+                                               const float *w_global_scale_f32, const uint16_t *x_bf16,
+                                               const int32_t *expert_offsets, const int32_t *sorted_token,
+                                               uint16_t *y_bf16, int E, int A, int n_tokens, int N, int K,
+                                               int swiglu, cudaStream_t stream) {
+    if (!w_packed || !w_scale_e4m3 || !w_global_scale_f32 || !x_bf16 || !expert_offsets || !sorted_token || !y_bf16)
+        return fail(NVFP4_ERR_INVALID_ARG, "null pointer argument");
+    if (E < 1 || A < 0 || n_tokens < 1 || N < 1)
+        return fail(NVFP4_ERR_INVALID_ARG, "E = %d, A = %d, n_tokens = %d, N = %d out of range", E, A, n_tokens, N);
+    if (swiglu != 0 && swiglu != 1) return fail(NVFP4_ERR_INVALID_ARG, "swiglu must be 0 or 1");
+    if (N % 16 != 0) return fail(NVFP4_ERR_INVALID_ARG, "N = %d must be a multiple of 16", N);
+    if (K < 32 || K % 32 != 0 || K > kMoeMaxK)
+        return fail(NVFP4_ERR_INVALID_ARG, "K = %d must be a multiple of 32 in [32, %d]", K, kMoeMaxK);
+    if ((long long)E * N > (1ll << 31) || (long long)A * N > (1ll << 40))
+        return fail(NVFP4_ERR_INVALID_ARG, "E * N or A * N too large");
+    if (!aligned16(w_packed) || !aligned16(w_scale_e4m3) || !aligned16(x_bf16) ||
+        (reinterpret_cast<uintptr_t>(y_bf16) & 1u) != 0)
+        return fail(NVFP4_ERR_MISALIGNED, "weights, scales and X must be 16-byte aligned");
+    if (A == 0) return NVFP4_OK;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    DeviceState *d = nullptr;
+    nvfp4_status st = device_state(dev, &d);
+    if (st != NVFP4_OK) return st;
+    MoeParams p;
+    p.w = w_packed;
+    p.s = w_scale_e4m3;
+    p.gs = w_global_scale_f32;
+    p.x = x_bf16;
+    p.off = expert_offsets;
+    p.tok = sorted_token;
+    p.y = y_bf16;
+    p.err = d->err_word;
+    p.E = E;
+    p.A = A;
+    p.ntok = n_tokens;
+    p.N = N;
+    p.K = K;
+    p.swiglu = swiglu;
+    const int out_rows = swiglu ? N / 2 : N;
+    p.rows_per_cta = moe_rows_per_cta(K, swiglu != 0, d->smem_optin);
+    if (p.rows_per_cta == 0)
+        return fail(NVFP4_ERR_UNSUPPORTED, "K = %d: the staged tokens and 16 weight rows do not fit shared memory", K);
+    p.row_groups = (out_rows + p.rows_per_cta - 1) / p.rows_per_cta;
+    if ((long long)E * p.row_groups > 0x7FFFFFFF) return fail(NVFP4_ERR_INVALID_ARG, "too many experts x rows");
+    if ((e = launch_moe(p, stream)) != cudaSuccess) return cuda_fail(e, "grouped expert kernel launch");
+    return NVFP4_OK;
+}
+
 extern "C" nvfp4_status nvfp4_device_error(cudaStream_t stream, int *code) {
     if (!code) return fail(NVFP4_ERR_INVALID_ARG, "null code pointer");
     *code = 0;
@@ -620,7 +672,7 @@ extern "C" nvfp4_status nvfp4_device_error(cudaStream_t stream, int *code) {
     const unsigned zero = 0;
     cudaMemcpy(d->err_word, &zero, sizeof zero, cudaMemcpyHostToDevice);
     if ((word & 7u) == 0)
-        return fail(NVFP4_ERR_DEVICE_INPUT, "a kernel met an input it cannot encode (error word 0x%x)", word);
+        return fail(NVFP4_ERR_DEVICE_INPUT, "a kernel met an input it cannot use (error word 0x%x)", word);
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         for (auto &w : g_workspaces)

@@ -40,6 +40,26 @@ struct StreamParams {
     int swiglu;          // tcgen05 only: rows 2f, 2f+1 are gate_f, up_f; y is h[n][N/2] = silu(gate) * up
 };
 
+// Grouped read-once GEMV over routed experts (moe_gemv.cu).
+struct MoeParams {
+    const uint8_t *w;   // [E][N][K/2]
+    const uint8_t *s;   // [E][N][K/16]
+    const float *gs;    // [E] global scales
+    const uint16_t *x;  // [ntok][K] bf16
+    const int *off;     // [E + 1] assignment offsets per expert
+    const int *tok;     // [A] token of each assignment, grouped by expert
+    uint16_t *y;        // [A][N] (or [A][N/2] with swiglu)
+    unsigned *err;      // device error word
+    int E, A, ntok, N, K, swiglu;
+    int rows_per_cta;   // output rows (gate/up pairs with swiglu) per CTA
+    int row_groups;     // CTAs per expert
+};
+constexpr int kMoeMaxK = 7168;
+int moe_smem_bytes(int K, int rows_per_cta, bool swiglu);
+int moe_rows_per_cta(int K, bool swiglu, int smem_optin);  // 0: K too large for shared memory
+cudaError_t moe_set_smem_limit(int smem_optin);
+cudaError_t launch_moe(const MoeParams &p, cudaStream_t stream);
+
 struct GenericParams {
     const uint8_t *w;
     const uint8_t *s;

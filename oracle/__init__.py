@@ -13,6 +13,8 @@ Parity status of each function (pins are in ``tests/test_oracle.py``):
     bfloat16 conversions, exact rational rounding).
   - gemv / gemv_rows / gemv_points: pinned (hand-worked golden cases, brute
     force against a dense numpy float64 reconstruction, invariants).
+  - moe_grouped: composition of gemv / gemv_swiglu per routed assignment
+    (pinned through them; routing semantics pinned in tests).
   - swiglu / gemv_swiglu: pinned (tabulated sigmoid values, the interleaved
     layout against two separate projections, special cases).
   - quantize: pinned against its definition (hand-derived golden codes, an
@@ -201,4 +203,24 @@ def gemv_swiglu(packed, scale, g, x):
     """Gate/up projection (rows 2f = gate f, 2f+1 = up f) followed by SwiGLU: (h64, h16) [n, F]."""
     y64, _ = gemv(packed, scale, g, x)
     return swiglu(y64)
+
+
+# ---------------------------------------------------------- routed experts
+def moe_grouped(packed, scale, g, x, expert_offsets, sorted_token, swiglu=False):
+    """Per assignment j of expert e (offsets[e] <= j < offsets[e+1]): the expert's
+    projection (or gate/up + SwiGLU) of token sorted_token[j].  packed [E][N][K/2],
+    scale [E][N][K/16], g [E], x uint16 [n][K].  Returns (y64, y16) [A][N or N/2]."""
+    E, N = packed.shape[0], packed.shape[1]
+    A = int(expert_offsets[-1])
+    width = N // 2 if swiglu else N
+    y64 = np.zeros((A, width), dtype=np.float64)
+    y16 = np.zeros((A, width), dtype=np.uint16)
+    for e in range(E):
+        a0, a1 = int(expert_offsets[e]), int(expert_offsets[e + 1])
+        if a1 <= a0:
+            continue
+        xe = np.ascontiguousarray(x[np.asarray(sorted_token[a0:a1], dtype=np.int64)])
+        fn = gemv_swiglu if swiglu else gemv
+        y64[a0:a1], y16[a0:a1] = fn(packed[e], scale[e], float(g[e]), xe)
+    return y64, y16
 

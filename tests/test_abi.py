@@ -68,6 +68,21 @@ def test_validation_errors_without_gpu():
         nv.nvfp4_quantize_ref(w)
 
 
+def test_grouped_expert_validation_without_gpu():
+    L = nv.lib()
+    a = ctypes.c_void_p(4096)
+    f = L.nvfp4_moe_gemv_grouped
+    assert f(None, a, a, a, a, a, a, 4, 8, 2, 64, 256, 0, None) == nv.NVFP4_ERR_INVALID_ARG
+    assert f(a, a, a, a, a, a, a, 0, 8, 2, 64, 256, 0, None) == nv.NVFP4_ERR_INVALID_ARG      # E
+    assert f(a, a, a, a, a, a, a, 4, 8, 2, 64, 240, 0, None) == nv.NVFP4_ERR_INVALID_ARG      # K % 32
+    assert f(a, a, a, a, a, a, a, 4, 8, 2, 64, 8192, 0, None) == nv.NVFP4_ERR_INVALID_ARG     # K too large
+    assert f(a, a, a, a, a, a, a, 4, 8, 2, 72, 256, 1, None) == nv.NVFP4_ERR_INVALID_ARG      # N % 16
+    assert f(a, a, a, a, a, a, a, 4, 8, 2, 64, 256, 2, None) == nv.NVFP4_ERR_INVALID_ARG      # swiglu flag
+    b = ctypes.c_void_p(4096 + 8)
+    assert f(b, a, a, a, a, a, a, 4, 8, 2, 64, 256, 0, None) == nv.NVFP4_ERR_MISALIGNED
+    assert f(a, a, a, a, a, a, a, 4, 0, 2, 64, 256, 0, None) == nv.NVFP4_OK                  # no assignment
+
+
 def test_device_quantizer_validation_without_gpu():
     """nvfp4_quantize / nvfp4_quantize_bf16 reject bad arguments before any CUDA call."""
     L = nv.lib()

@@ -387,3 +387,24 @@ def test_gemv_swiglu_interleaving_matches_two_projections():
     # swapping the roles changes the result (silu is not symmetric)
     swapped = u64 / (1.0 + np.exp(-u64)) * g64
     assert not np.allclose(h64, swapped, rtol=1e-3, atol=1e-3)
+
+
+# ----------------------------------------------------------- routed experts
+def test_moe_grouped_routing_semantics():
+    rng = np.random.Generator(np.random.PCG64(31))
+    E, N, K, n = 3, 40, 64, 5
+    ws = [oracle.quantize(rng.standard_normal((N, K), dtype=np.float32)) for _ in range(E)]
+    packed = np.stack([w[0] for w in ws]); scale = np.stack([w[1] for w in ws])
+    g = np.array([w[2] for w in ws], dtype=np.float32)
+    x = synth.activations_bf16(n, K, seed=32)
+    # expert 0: tokens 4, 1; expert 1: none; expert 2: tokens 0, 4, 2
+    off = np.array([0, 2, 2, 5], dtype=np.int32)
+    tok = np.array([4, 1, 0, 4, 2], dtype=np.int32)
+    y64, y16 = oracle.moe_grouped(packed, scale, g, x, off, tok)
+    for j, (e, t) in enumerate([(0, 4), (0, 1), (2, 0), (2, 4), (2, 2)]):
+        r64, r16 = oracle.gemv(packed[e], scale[e], float(g[e]), x[t:t + 1])
+        assert np.array_equal(y64[j], r64[0]) and np.array_equal(y16[j], r16[0])
+    # one expert holding every token is the plain batched projection
+    a64, _ = oracle.moe_grouped(packed[:1], scale[:1], g[:1], x, np.array([0, n], np.int32), np.arange(n, dtype=np.int32))
+    b64, _ = oracle.gemv(packed[0], scale[0], float(g[0]), x)
+    assert np.array_equal(a64, b64)
