@@ -125,6 +125,21 @@ def synth_bf16_weights(torch, N, K, seed, dev):
     return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
 
 
+# ------------------------------------------------------------ replicas
+def max_over_ranks(torch, dist, value, device):
+    """The slowest rank's time (all ranks receive it); `value` itself on one process."""
+    if dist is None:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world, step_bytes, ms_per_step):
+    """Whole-job throughput: every rank moved step_bytes per step in the slowest rank's time."""
+    return world * step_bytes / (ms_per_step * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -308,14 +323,11 @@ def run_moe(args, torch, nv, rank, world, local_rank, wl_desc, cores):
     torch.cuda.synchronize()
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(torch, dist, ms, dev)
     if nv.nvfp4_device_error(stream) != 0:
         raise SystemExit("device error during the timed region")
     ms_per_step = ms / args.steps
-    value = world * mean_bytes / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(world, mean_bytes, ms_per_step)
     # end to end: X in from pinned host memory, Y out, every step
     e2e_steps = max(20, min(2000, args.steps // 10))
     with torch.cuda.stream(stream):
@@ -330,7 +342,7 @@ def run_moe(args, torch, nv, rank, world, local_rank, wl_desc, cores):
             y_host.copy_(y, non_blocking=True)
         b.record(stream)
     b.synchronize()
-    e2e_ms = a.elapsed_time(b) / e2e_steps
+    e2e_ms = max_over_ranks(torch, dist, a.elapsed_time(b) / e2e_steps, dev)
     hbm_peak, peak_kind = peaks()
     achieved = mean_bytes / (ms_per_step * 1e-3) / 1e9
     if dist is not None:
@@ -544,12 +556,9 @@ def main():
     barrier()
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(torch, dist, ms, dev)
     ms_per_step = ms / args.steps
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(world, step_bytes, ms_per_step)
     if nv.nvfp4_device_error(stream) != 0:
         raise SystemExit("device error during the timed region")
 
@@ -667,11 +676,8 @@ def main():
         b.record(stream)
     b.synchronize()
     e2e_ms = a.elapsed_time(b) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(torch, dist, e2e_ms, dev)
+    e2e_value = whole_job_gbs(world, step_bytes, e2e_ms)
 
     traffic, traffic_n = kernel_traffic(plan["variant"]) if not is_ffn else (None, None)
     achieved = step_bytes / (ms_per_step * 1e-3) / 1e9  # per GPU: algorithmic bytes per launch / launch time
