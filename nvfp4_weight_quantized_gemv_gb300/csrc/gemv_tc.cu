@@ -98,14 +98,22 @@ constexpr int kTcPartialFloats = kConsumerWarps * kSlotFloats;  // one partial t
 
 static_assert(kTcDCol + kTcIssuers * 2 * 16 <= (int)kTcTmemCols, "tensor memory");
 
-// barriers: full[S] empty[S] xloaded[KG] xfull[KG] afull[3][2] aempty[3][2] dfull[3][2] dempty[2] final[3] xreq
+// Each A buffer is handed from the dequant warps to its issuer, and back, in
+// kTcAParts parts of 256 / kTcAParts k (the lane-quarter warps of those k
+// quarters), so MMAs start once a part is converted and a part is refilled as
+// soon as its MMAs are done.  Two parts measured best (four: more commits and
+// barrier round trips per unit for no shorter cycle).
+constexpr int kTcAParts = 2;
+constexpr int kTcStepsPerPart = 16 / kTcAParts;  // MMA k-steps (16 k each) per part
+
+// barriers: full[S] empty[S] xloaded[KG] xfull[KG] afull[3][P] aempty[3][P] dfull[3][2] dempty[2] final[3] xreq
 __host__ __device__ constexpr int tc_barrier_count(int S, int KG) {
-    return 2 * S + 2 * KG + 4 * kTcABufs + 2 * kTcIssuers + 2 + kTcIssuers + 1;
+    return 2 * S + 2 * KG + 2 * kTcABufs * kTcAParts + 2 * kTcIssuers + 2 + kTcIssuers + 1;
 }
 // Weight stages requested before X: the rest of the ring is requested only
 // once the X warp has requested X, so that X does not queue behind a full
 // ring of weight traffic from this SM.
-constexpr int kTcStagesBeforeX = 4;
+constexpr int kTcStagesBeforeX = 2;
 constexpr int kTcXConverterWarps = kTcEpilogueWarps;  // the epilogue warps convert X before their epilogue work
 
 // Group g of `groups` k-groups over KC unit columns: first unit column and width.
@@ -232,9 +240,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t sEmpty = sFull + 8 * S;              // dequant warps done with W + scales, count 16
     const uint32_t sXLoaded = sEmpty + 8 * S;           // [unit column] bf16 X landed (TMA), one phase
     const uint32_t sXFull = sXLoaded + 8 * kg_max;      // [unit column] f16 X ready, count 5 (converter warps)
-    const uint32_t sAFull = sXFull + 8 * kg_max;        // [buffer][half], count 8
-    const uint32_t sAEmpty = sAFull + 16 * kTcABufs;    // [buffer][half], count 1 (commit)
-    const uint32_t sDFull = sAEmpty + 16 * kTcABufs;    // [issuer][segment buffer], count 1 (commit)
+    const uint32_t sAFull = sXFull + 8 * kg_max;        // [buffer][part], count = warps per part
+    const uint32_t sAEmpty = sAFull + 8 * kTcABufs * kTcAParts;   // [buffer][part], count 1 (commit)
+    const uint32_t sDFull = sAEmpty + 8 * kTcABufs * kTcAParts;   // [issuer][segment buffer], count 1 (commit)
     const uint32_t sDEmpty = sDFull + 16 * kTcIssuers;  // [segment buffer], count 4 (epilogue warps)
     const uint32_t sFinal = sDEmpty + 16;               // [issuer], count 1 (commit)
     const uint32_t sXReq = sFinal + 8 * kTcIssuers;     // X requested (X warp), count 1
@@ -272,8 +280,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(sXLoaded + 8 * s, 1);
             mbar_init(sXFull + 8 * s, kTcXConverterWarps);
         }
-        for (int b = 0; b < 2 * kTcABufs; ++b) {
-            mbar_init(sAFull + 8 * b, kTcDequantWarps / 2);
+        for (int b = 0; b < kTcABufs * kTcAParts; ++b) {
+            mbar_init(sAFull + 8 * b, kTcDequantWarps / kTcAParts);
             mbar_init(sAEmpty + 8 * b, 1);
         }
         for (int d = 0; d < 2 * kTcIssuers; ++d) mbar_init(sDFull + 8 * d, 1);
@@ -442,28 +450,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t a_tmem = tbase + a * kTcAColsPerUnit;
                     const unsigned par = (ib / kTcABufs) & 1;
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        // the two boxes (64 k each) of this half: tokens 8-15 are the next
+                    for (int part = 0; part < kTcAParts; ++part) {
+                        // descriptors of the part's 64-k boxes: tokens 8-15 are the next
                         // atom (T == 16) or the zero block (T == 8)
-                        uint64_t bd[2];
+                        constexpr int kBoxes = kTcStepsPerPart / 4;
+                        uint64_t bd[kBoxes];
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint32_t box = xbase + (uint32_t)(2 * half + h) * xbox;
+                        for (int h = 0; h < kBoxes; ++h) {
+                            const uint32_t box = xbase + (uint32_t)(part * kBoxes + h) * xbox;
                             bd[h] = tc::smem_desc_sw128(box, (T == 16) ? 1024u : (sZero - box));
                         }
-                        if (!mbar_wait_bounded(sAFull + 8 * (a * 2 + half), par)) {
+                        if (!mbar_wait_bounded(sAFull + 8 * (a * kTcAParts + part), par)) {
                             ok = false;
                             break;
                         }
                         tc::fence_after_sync();
 #pragma unroll
-                        for (int s = 8 * half; s < 8 * half + 8; ++s) {
+                        for (int s = part * kTcStepsPerPart; s < (part + 1) * kTcStepsPerPart; ++s) {
                             // k-step s: box s/4, bytes 32*(s%4) into each 128-byte row (the
                             // start-address field counts 16-byte units and does not carry)
-                            const uint64_t bdesc = bd[(s >> 2) & 1] + (uint64_t)(2 * (s & 3));
+                            const uint64_t bdesc = bd[(s >> 2) % kBoxes] + (uint64_t)(2 * (s & 3));
                             tc::mma_f16_ts(d_tmem, a_tmem + s * 8, bdesc, idesc, !(first && s == 0));
                         }
-                        tc::commit(sAEmpty + 8 * (a * 2 + half));
+                        tc::commit(sAEmpty + 8 * (a * kTcAParts + part));
                     }
                     if (!ok) break;
                     first = false;
@@ -483,7 +492,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int e = warp - kTcWarpDequant0;  // 0..15
         const int lq = warp & 3;               // tensor-memory lane quarter this warp may access
         const int kq = e >> 2;                 // which 64-k quarter of the unit
-        const int half = kq >> 1;
+        const int part = kq / (4 / kTcAParts);  // this warp's part of every A buffer
         const int r = 32 * lq + lane;          // row within the unit
         const uint32_t lane_bits = (uint32_t)(32 * lq) << 16;
         // this lane's 64 k of row r in stage 0: two swizzled 16-byte chunks of
@@ -512,7 +521,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t s01 = e4m3x2_to_f16x2(sv), s23 = e4m3x2_to_f16x2(sv >> 16);
             const uint32_t sc[4] = {dup_lo(s01), dup_hi(s01), dup_lo(s23), dup_hi(s23)};
             if (i >= kTcABufs &&
-                __any_sync(0xffffffffu, !mbar_wait_bounded(sAEmpty + 8 * (ab * 2 + half), apar))) {
+                __any_sync(0xffffffffu, !mbar_wait_bounded(sAEmpty + 8 * (ab * kTcAParts + part), apar))) {
                 ok = false;
                 break;
             }
@@ -533,7 +542,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc::wait_st();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(sAFull + 8 * (ab * 2 + half));
+            if (lane == 0) mbar_arrive(sAFull + 8 * (ab * kTcAParts + part));
             if (++ab == kTcABufs) {  // next round R = i / 3 + 1 waits for the phase of round R - 1
                 ab = 0;
                 apar ^= 1u;
