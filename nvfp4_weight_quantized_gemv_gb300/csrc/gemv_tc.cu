@@ -27,23 +27,25 @@
 // past n zero-filled) and the epilogue warps convert it in place.  No
 // separate conversion kernel or X buffer in global memory.
 //
-// Warp roles (800 threads, one CTA per SM):
+// Warp roles (832 threads, one CTA per SM):
 //   warp 0       weight producer: 2D TMA loads of the unit's W tile
 //                (128B-swizzled) and scale tile into a ring of S stages.
 //   warp 1       X loads (see above).
-//   warps 2-4    MMA issuers.  Unit i is multiplied by issuer i % 3 out of
-//                tensor-memory A buffer i % 3, so every barrier of a buffer
-//                has one waiter that sees each of its phases.  16 x
-//                tcgen05.mma.kind::f16 per unit, M = 128 weight rows, N = 16
-//                token columns, K = 16; A from tensor memory, B (= X) from
-//                shared memory, fp32 accumulators in tensor memory per
-//                (issuer, row-block segment buffer).
-//   warps 5-20   dequantise: thread = weight row; warp (lane quarter q, k
+//   warps 2-5    MMA issuers.  Unit i uses tensor-memory A buffer i % 2;
+//                each buffer has two issuers, one per 128-k half, each with
+//                its own fp32 accumulators in tensor memory per row-block
+//                segment buffer (summed by the epilogue in fixed order), so
+//                the two halves' MMAs run concurrently and every barrier of
+//                a buffer half has one waiter that sees each of its phases.
+//                8 x tcgen05.mma.kind::f16 per half unit, M = 128 weight
+//                rows, N = 16 token columns, K = 16; A from tensor memory,
+//                B (= X) from shared memory.
+//   warps 6-21   dequantise: thread = weight row; warp (lane quarter q, k
 //                quarter j) turns rows 32q..32q+31, k 64j..64j+63 of every
 //                unit into f16 (E2M1 cvt times the E4M3 block scale: exact)
 //                and stores them with one tcgen05.st.  Each A buffer is
 //                handed over in two 128-k halves.
-//   warps 21-24  X conversion (bf16 -> f16 x 2^-8 in shared memory, unit by
+//   warps 22-25  X conversion (bf16 -> f16 x 2^-8 in shared memory, unit by
 //                unit in the order the CTA uses them), then the epilogue:
 //                per finished row-block segment, tcgen05.ld of the
 //                issuers' accumulators, summed in a fixed order, then either
@@ -78,19 +80,20 @@ namespace {
 constexpr int kTcUnitK = 256;                    // k per unit (128 packed bytes per row)
 constexpr int kTcWBytes = kUnitRows * 128;       // 16384
 constexpr int kTcSBytes = kUnitRows * 16;        // 2048
-constexpr int kTcABufs = 3;                      // A buffers (= issuers), 128 columns each
+constexpr int kTcABufs = 2;                      // A buffers, 128 columns each
+constexpr int kTcIssuersPerBuf = 2;              // MMA issuers per A buffer (each takes 1 / this of its parts)
 constexpr int kTcAColsPerUnit = kTcUnitK / 2;    // two f16 per 32-bit column
-constexpr int kTcIssuers = kTcABufs;
-constexpr int kTcDCol = kTcABufs * kTcAColsPerUnit;  // 384: accumulators [issuer 3][segment buffer 2][16 cols]
+constexpr int kTcIssuers = kTcABufs * kTcIssuersPerBuf;
+constexpr int kTcDCol = kTcABufs * kTcAColsPerUnit;  // accumulators [issuer][segment buffer 2][16 cols] from here
 constexpr uint32_t kTcTmemCols = 512;
 constexpr int kTcWarpProducer = 0;
 constexpr int kTcWarpX = 1;
-constexpr int kTcWarpIssuer0 = kTcWarpX + 1;                    // issuers: warps 2..4
-constexpr int kTcWarpDequant0 = kTcWarpIssuer0 + kTcIssuers;    // dequant: warps 5..20
+constexpr int kTcWarpIssuer0 = kTcWarpX + 1;                    // issuers: warps 2 ..
+constexpr int kTcWarpDequant0 = kTcWarpIssuer0 + kTcIssuers;    // dequant: the next 16 warps
 constexpr int kTcDequantWarps = 16;
 constexpr int kTcWarpEpilogue0 = kTcWarpDequant0 + kTcDequantWarps;  // epilogue: warps 21..24
 constexpr int kTcEpilogueWarps = 4;
-constexpr int kTcThreads = (kTcWarpEpilogue0 + kTcEpilogueWarps) * 32;  // 800
+constexpr int kTcThreads = (kTcWarpEpilogue0 + kTcEpilogueWarps) * 32;  // 832
 constexpr float kTcXScale = 1.0f / 256.0f;       // 2^-8 applied to X before the f16 cast
 constexpr float kTcXUnscale = 256.0f;
 constexpr unsigned kDevErrXRange = 8u;           // some |x| >= 65520 * 2^8
@@ -105,6 +108,8 @@ static_assert(kTcDCol + kTcIssuers * 2 * 16 <= (int)kTcTmemCols, "tensor memory"
 // barrier round trips per unit for no shorter cycle).
 constexpr int kTcAParts = 2;
 constexpr int kTcStepsPerPart = 16 / kTcAParts;  // MMA k-steps (16 k each) per part
+constexpr int kTcPartsPerIssuer = kTcAParts / kTcIssuersPerBuf;
+static_assert(kTcPartsPerIssuer * kTcIssuersPerBuf == kTcAParts, "issuers split a buffer's parts evenly");
 
 // barriers: full[S] empty[S] xloaded[KG] xfull[KG] afull[3][P] aempty[3][P] dfull[3][2] dempty[2] final[3] xreq
 __host__ __device__ constexpr int tc_barrier_count(int S, int KG) {
@@ -423,7 +428,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else if (warp < kTcWarpDequant0) {
         // ---------------------------------------------------------- MMA issuers
-        const int a = warp - kTcWarpIssuer0;  // A buffer / accumulator of this issuer
+        const int w = warp - kTcWarpIssuer0;  // accumulator of this issuer
+        const int a = w / kTcIssuersPerBuf;   // its A buffer: units i with i % kTcABufs == a
+        const int p0 = (w % kTcIssuersPerBuf) * kTcPartsPerIssuer;  // its parts of each unit
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_f16_f32(kUnitRows, 16);
             bool ok = true;
@@ -437,10 +444,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t d_tmem = tbase + kTcDCol + a * 32 + sb * 16;
+                const uint32_t d_tmem = tbase + kTcDCol + w * 32 + sb * 16;
                 bool first = true;
-                int ib = i + ((a - i % kTcIssuers) + kTcIssuers) % kTcIssuers;  // first unit of this issuer
-                for (; ib <= iend; ib += kTcIssuers) {
+                int ib = i + ((a - i % kTcABufs) + kTcABufs) % kTcABufs;  // first unit of this issuer
+                for (; ib <= iend; ib += kTcABufs) {
                     const int l = kl + (ib - i);  // unit column within the group
                     if (!mbar_wait_bounded(sXFull + 8 * l, 0)) {
                         ok = false;
@@ -450,7 +457,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t a_tmem = tbase + a * kTcAColsPerUnit;
                     const unsigned par = (ib / kTcABufs) & 1;
 #pragma unroll
-                    for (int part = 0; part < kTcAParts; ++part) {
+                    for (int part = p0; part < p0 + kTcPartsPerIssuer; ++part) {
                         // descriptors of the part's 64-k boxes: tokens 8-15 are the next
                         // atom (T == 16) or the zero block (T == 8)
                         constexpr int kBoxes = kTcStepsPerPart / 4;
@@ -466,11 +473,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         tc::fence_after_sync();
 #pragma unroll
-                        for (int s = part * kTcStepsPerPart; s < (part + 1) * kTcStepsPerPart; ++s) {
-                            // k-step s: box s/4, bytes 32*(s%4) into each 128-byte row (the
-                            // start-address field counts 16-byte units and does not carry)
-                            const uint64_t bdesc = bd[(s >> 2) % kBoxes] + (uint64_t)(2 * (s & 3));
-                            tc::mma_f16_ts(d_tmem, a_tmem + s * 8, bdesc, idesc, !(first && s == 0));
+                        for (int j = 0; j < kTcStepsPerPart; ++j) {
+                            // k-step s = part * steps + j: box s/4, bytes 32*(s%4) into each
+                            // 128-byte row (the start-address field counts 16-byte units and
+                            // does not carry)
+                            const int s = part * kTcStepsPerPart + j;
+                            const uint64_t bdesc = bd[j >> 2] + (uint64_t)(2 * (j & 3));
+                            tc::mma_f16_ts(d_tmem, a_tmem + s * 8, bdesc, idesc, !(first && part == p0 && j == 0));
                         }
                         tc::commit(sAEmpty + 8 * (a * kTcAParts + part));
                     }
@@ -478,13 +487,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     first = false;
                 }
                 // every issuer closes every segment, so the epilogue sees each phase
-                tc::commit(sDFull + 8 * (a * 2 + sb));
+                tc::commit(sDFull + 8 * (w * 2 + sb));
                 kl = 0;
                 i = iend + 1;
             }
             if (!ok) atomicOr(p.err, kDevErrTimeoutFull);
-            tc::commit(sFinal + 8 * a);
-            if (!mbar_wait_bounded(sFinal + 8 * a, 0)) atomicOr(p.err, kDevErrTimeoutDrain);
+            tc::commit(sFinal + 8 * w);
+            if (!mbar_wait_bounded(sFinal + 8 * w, 0)) atomicOr(p.err, kDevErrTimeoutDrain);
         }
         __syncwarp();
     } else if (warp < kTcWarpEpilogue0) {
@@ -543,7 +552,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(sAFull + 8 * (ab * kTcAParts + part));
-            if (++ab == kTcABufs) {  // next round R = i / 3 + 1 waits for the phase of round R - 1
+            if (++ab == kTcABufs) {  // next round R = i / kTcABufs + 1 waits for the phase of round R - 1
                 ab = 0;
                 apar ^= 1u;
             }
@@ -577,8 +586,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float v[16];
             bool have = false;
 #pragma unroll
-            for (int q = 0; q < kTcIssuers; ++q) {  // fixed order: issuers 0, 1, 2
-                const bool contributed = len >= kTcIssuers || ((q - i % kTcIssuers + kTcIssuers) % kTcIssuers) < len;
+            for (int q = 0; q < kTcIssuers; ++q) {  // fixed order: issuer 0, 1, ...
+                const int qb = q / kTcIssuersPerBuf;  // the A buffer (unit residue) of issuer q
+                const bool contributed = len >= kTcABufs || ((qb - i % kTcABufs + kTcABufs) % kTcABufs) < len;
                 if (!contributed) continue;
                 uint32_t d[16];
                 tc::ld_32x32b_x16(tbase + lane_bits + kTcDCol + q * 32 + sb * 16, d);
