@@ -300,9 +300,19 @@ def run_moe(args, torch, nv, rank, world, local_rank, wl_desc, cores):
         with torch.cuda.graph(gph, stream=stream):
             step(i, stream)
         graphs.append(gph)
+    cycle = torch.cuda.CUDAGraph()  # the R routings' steps chained in one graph launch
+    with torch.cuda.graph(cycle, stream=stream):
+        for i in range(R):
+            step(i, stream)
+
+    def replay_steps(k):
+        for _ in range(k // R):
+            cycle.replay()
+        for j in range(k % R):
+            graphs[j].replay()
+
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            graphs[i % R].replay()
+        replay_steps(-(-args.warmup // R) * R)
     stream.synchronize()
     if nv.nvfp4_device_error(stream) != 0:
         raise SystemExit("device error during warm-up")
@@ -314,8 +324,7 @@ def run_moe(args, torch, nv, rank, world, local_rank, wl_desc, cores):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        for i in range(args.steps):
-            graphs[i % R].replay()
+        replay_steps(args.steps)
         ev1.record(stream)
     ev1.synchronize()
     if dist is not None:
@@ -327,6 +336,9 @@ def run_moe(args, torch, nv, rank, world, local_rank, wl_desc, cores):
     if nv.nvfp4_device_error(stream) != 0:
         raise SystemExit("device error during the timed region")
     ms_per_step = ms / args.steps
+    # the timed steps' own bytes: whole cycles of the R routings, then the first steps % R
+    timed_bytes = (args.steps // R) * sum(step_bytes) + sum(step_bytes[:args.steps % R])
+    mean_bytes = timed_bytes / args.steps
     value = whole_job_gbs(world, mean_bytes, ms_per_step)
     # end to end: X in from pinned host memory, Y out, every step
     e2e_steps = max(20, min(2000, args.steps // 10))
@@ -522,6 +534,20 @@ def main():
         with torch.cuda.graph(gph, stream=stream):
             enqueue_step(stream)
         graphs.append(gph)
+    # all phases in one graph, as a served decode step captures all its layers:
+    # consecutive steps then chain inside one graph launch
+    cycle = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cycle, stream=stream):
+        for _ in range(phases):
+            enqueue_step(stream)
+
+    def replay_steps(k):
+        # exactly k steps: whole cycles, then the first k % phases phases
+        for _ in range(k // phases):
+            cycle.replay()
+        for j in range(k % phases):
+            graphs[j].replay()
+
     plan = nv.nvfp4_gemv_plan(calls[-1][1], *SHAPES[calls[-1][0]], variant=variant, tiling=tiling)
     def launches(plan_info):
         # tcgen05 path: GEMV and split-row reduction per pass
@@ -535,10 +561,9 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    # warm-up
+    # warm-up (whole cycles, so the timed region starts at phase 0 on fresh weight copies)
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            graphs[i % phases].replay()
+        replay_steps(-(-args.warmup // phases) * phases)
     stream.synchronize()
     if nv.nvfp4_device_error(stream) != 0:
         raise SystemExit("device error during warm-up")
@@ -549,8 +574,7 @@ def main():
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        for i in range(args.steps):
-            graphs[i % phases].replay()
+        replay_steps(args.steps)
         ev1.record(stream)
     ev1.synchronize()
     barrier()
