@@ -286,10 +286,13 @@ nvfp4_status nvfp4_quantize_bf16(const uint16_t *w_bf16, int N, int K, uint8_t *
  *            copies in flight at exit) after about 2 s;
  *   8        a GEMV met |x| >= 65520 * 2^8 (see nvfp4_gemv_batched);
  *   16       the device quantizer met a non-finite weight;
- *   32       the grouped expert GEMV met bad routing data.
+ *   32       the grouped expert GEMV met bad routing data;
+ *   64       the tcgen05 GEMV found its dynamic shared memory off a 1024-byte
+ *            boundary and computed nothing (a platform fault, never expected).
  * Returns NVFP4_ERR_DEVICE_TIMEOUT when any of bits 1, 2, 4 is set (the
  * library then also re-zeroes its own workspaces so later calls start clean),
- * else NVFP4_ERR_DEVICE_INPUT when bit 8, 16 or 32 is set, else NVFP4_OK. */
+ * else NVFP4_ERR_UNSUPPORTED when bit 64 is set, else NVFP4_ERR_DEVICE_INPUT
+ * when bit 8, 16 or 32 is set, else NVFP4_OK. */
 nvfp4_status nvfp4_device_error(cudaStream_t stream, int *code);
 
 /* Message for the last non-OK status returned on this thread ("" if none). */

@@ -671,6 +671,9 @@ extern "C" nvfp4_status nvfp4_device_error(cudaStream_t stream, int *code) {
     if (word == 0) return NVFP4_OK;
     const unsigned zero = 0;
     cudaMemcpy(d->err_word, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if ((word & 7u) == 0 && (word & 64u) != 0)
+        return fail(NVFP4_ERR_UNSUPPORTED, "the GEMV found its dynamic shared memory off a 1024-byte boundary "
+                    "and computed nothing (error word 0x%x)", word);
     if ((word & 7u) == 0)
         return fail(NVFP4_ERR_DEVICE_INPUT, "a kernel met an input it cannot use (error word 0x%x)", word);
     {

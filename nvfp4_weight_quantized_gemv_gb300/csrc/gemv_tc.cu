@@ -58,11 +58,13 @@
 // word (the output is then not meaningful).
 //
 // Programmatic dependent launch: the kernel lets the next kernel on the stream
-// (the split-row reduction) launch once all its CTAs have finished their
-// epilogue work, and it starts its own weight stream
-// before the kernel ahead of it has finished; X, the global scale, the
-// workspace and Y are touched only after griddepcontrol.wait.  Weights and
-// scales are therefore read as constants of the call.
+// (the split-row reduction) launch as soon as its CTAs are set up -- the
+// reduction needs no shared memory and few registers, so its CTAs sit next to
+// the GEMV CTAs, waiting for this grid, and never keep the next call's GEMV
+// off an SM -- and it starts its own weight stream before the kernel ahead of
+// it has finished; X, the global scale, the workspace and Y are touched only
+// after griddepcontrol.wait.  Weights and scales are therefore read as
+// constants of the call.
 //
 // Every wait is bounded (2 s of %globaltimer); on a timeout the kernel sets
 // the device error word, skips the remaining work, waits (bounded) for its
@@ -91,12 +93,13 @@ constexpr int kTcWarpX = 1;
 constexpr int kTcWarpIssuer0 = kTcWarpX + 1;                    // issuers: warps 2 ..
 constexpr int kTcWarpDequant0 = kTcWarpIssuer0 + kTcIssuers;    // dequant: the next 16 warps
 constexpr int kTcDequantWarps = 16;
-constexpr int kTcWarpEpilogue0 = kTcWarpDequant0 + kTcDequantWarps;  // epilogue: warps 21..24
+constexpr int kTcWarpEpilogue0 = kTcWarpDequant0 + kTcDequantWarps;  // epilogue: warps 22..25
 constexpr int kTcEpilogueWarps = 4;
 constexpr int kTcThreads = (kTcWarpEpilogue0 + kTcEpilogueWarps) * 32;  // 832
 constexpr float kTcXScale = 1.0f / 256.0f;       // 2^-8 applied to X before the f16 cast
 constexpr float kTcXUnscale = 256.0f;
 constexpr unsigned kDevErrXRange = 8u;           // some |x| >= 65520 * 2^8
+constexpr unsigned kDevErrSmemBase = 64u;        // dynamic shared memory not 1024-byte aligned
 constexpr int kTcPartialFloats = kConsumerWarps * kSlotFloats;  // one partial tile slot: 128 rows x 16 tokens
 
 static_assert(kTcDCol + kTcIssuers * 2 * 16 <= (int)kTcTmemCols, "tensor memory");
@@ -111,7 +114,8 @@ constexpr int kTcStepsPerPart = 16 / kTcAParts;  // MMA k-steps (16 k each) per 
 constexpr int kTcPartsPerIssuer = kTcAParts / kTcIssuersPerBuf;
 static_assert(kTcPartsPerIssuer * kTcIssuersPerBuf == kTcAParts, "issuers split a buffer's parts evenly");
 
-// barriers: full[S] empty[S] xloaded[KG] xfull[KG] afull[3][P] aempty[3][P] dfull[3][2] dempty[2] final[3] xreq
+// barriers: full[S] empty[S] xloaded[KG] xfull[KG] afull[B][P] aempty[B][P] dfull[I][2] dempty[2] final[I] xreq
+// (B A buffers, P parts, I issuers)
 __host__ __device__ constexpr int tc_barrier_count(int S, int KG) {
     return 2 * S + 2 * KG + 2 * kTcABufs * kTcAParts + 2 * kTcIssuers + 2 + kTcIssuers + 1;
 }
@@ -199,10 +203,12 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, uint32_t 
 // X area: kg_max units x 16 token rows x 512 B -- the f16 X for T = 16, or
 // the f16 X (8 rows) plus the bf16 staging (8 rows) for T = 8: the same size,
 // so the plan does not depend on n.
+// The dynamic shared memory starts 1024-byte aligned (the kernel checks it),
+// so no alignment slack is reserved: the GEMV then leaves room on its SM for a
+// reduction CTA (its 1 KB of reserved shared memory).
 int tc_smem_bytes(int stages, int T, int kg_max) {
     (void)T;
-    return 1024 + stages * (kTcWBytes + kTcSBytes) + kg_max * 16 * 512 + 1024 + 8 * tc_barrier_count(stages, kg_max) +
-           64;
+    return stages * (kTcWBytes + kTcSBytes) + kg_max * 16 * 512 + 1024 + 8 * tc_barrier_count(stages, kg_max) + 64;
 }
 
 void tc_group_host(int g, int groups, int KC, int *kstart, int *kg) { tc_group(g, groups, KC, kstart, kg); }
@@ -212,10 +218,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
                    const __grid_constant__ CUtensorMap tmap_x, const StreamParams p, const TcPartition part) {
     static_assert(T == 8 || T == 16, "staged tokens");
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_addr = smem_u32(smem_raw);
-    const uint32_t sW = (raw_addr + 1023u) & ~1023u;
-    uint8_t *const base = smem_raw + (sW - raw_addr);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t sW = smem_u32(smem_raw);
+    if (sW & 1023u) {  // the swizzled tiles need a 1024-byte aligned base; never expected
+        griddep_wait();
+        if (threadIdx.x == 0) atomicOr(p.err, kDevErrSmemBase);
+        return;
+    }
+    uint8_t *const base = smem_raw;
     const int S = p.stages;                              // even (every dequant warp sees every phase)
     const int KC = p.KC;
     const int G = part.groups;
@@ -306,6 +316,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tbase = misc[0];
+    // The reduction may launch now: its CTAs fit next to this one and only
+    // wait (griddepcontrol.wait) until this grid has finished.
+    if (threadIdx.x == 0) griddep_launch_dependents();
 
     // X conversion by the epilogue warps (converter cv = 0..3), unit column
     // by unit column in the order the CTA uses them; each warp arrives on a
@@ -618,10 +631,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             kl = 0;
             ++rb;
         }
-        // The reduction kernel may launch once every CTA is here: launched
-        // earlier, its CTAs would sit on SMs (waiting for this grid) that the
-        // next call's GEMV CTAs need.
-        if (warp == kTcWarpEpilogue0 && lane == 0) griddep_launch_dependents();
     }
 
     tc::fence_before_sync();
@@ -635,71 +644,90 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // Split row blocks: one CTA per row block, one thread per row.  The parts of
 // row block rb are the unit ranges of CTAs [ca, cb] of every k-group, taken
 // in CTA order; part (CTA c) sits in c's slot for rb (c's partial tiles are
-// indexed by row block from its first one).  Each thread fetches its row of
-// kTcReduceChunk parts at a time into registers (all those loads in flight
-// together: one memory round trip per chunk), then sums them in order; no
-// shared memory, so the kernel never keeps the next GEMV off an SM.  Row
-// blocks finished whole by the GEMV (a single part) are skipped.  Index
-// arithmetic is 32-bit: the planner keeps row_blocks * KC * (grid + 1) below
-// 2^32.
-__global__ void __launch_bounds__(kUnitRows) tc_reduce_kernel(const StreamParams p, const TcPartition part, const int T) {
-    __shared__ int slots[kTcMaxParts];
-    __shared__ int nparts;
-    griddep_launch_dependents();
-    const unsigned rb = blockIdx.x;
-    const int G = part.groups, KC = p.KC;
-    if (threadIdx.x == 0) {
-        int np = 0;
-        for (int g = 0; g < G; ++g) {
-            int ks, kg;
-            tc_group(g, G, KC, &ks, &kg);
-            const unsigned cs = part.cstart[g], cg = part.cstart[g + 1] - cs;
-            const unsigned u = (unsigned)part.row_blocks * kg;
-            const unsigned ca = ((rb * kg + 1) * cg - 1) / u, cb = ((rb * kg + kg) * cg - 1) / u;
-            for (unsigned c = ca; c <= cb && np < kTcMaxParts; ++c) {
-                const unsigned rbf = (c * u / cg) / kg;  // that CTA's first row block
-                slots[np++] = (int)((cs + c) * part.max_seg + (rb - rbf));
-            }
-        }
-        nparts = np;
+// indexed by row block from its first one).  Each thread walks that list
+// itself and fetches its row of 32 / T parts at a time into registers (all
+// those loads in flight together: one memory round trip per chunk), then sums
+// them in order.  No shared memory and at most 64 registers a thread, so a
+// reduction CTA fits on an SM next to a GEMV CTA: it can be resident (and
+// waiting) before the GEMV finishes, and it never keeps the next call's GEMV
+// CTA off an SM.  Row blocks finished whole by the GEMV (a single part) are
+// skipped.  Index arithmetic is 32-bit: the planner keeps row_blocks * KC *
+// (grid + 1) below 2^32.
+struct TcPartCursor {  // walks the parts of one row block in (group, CTA) order
+    unsigned rb, g, c, cb, cs, cg, u, kg;
+    int G, KC;
+    __device__ void enter_group(const TcPartition &part) {
+        int ks, kgi;
+        tc_group((int)g, G, KC, &ks, &kgi);
+        kg = (unsigned)kgi;
+        cs = (unsigned)part.cstart[g];
+        cg = (unsigned)part.cstart[g + 1] - cs;
+        u = (unsigned)part.row_blocks * kg;
+        c = ((rb * kg + 1) * cg - 1) / u;
+        cb = ((rb * kg + kg) * cg - 1) / u;
     }
-    __syncthreads();
-    const int np = nparts;
+    __device__ unsigned parts_in_group() const { return cb - c + 1; }
+    // slot of the current part, then advance; call at most the number of parts times
+    __device__ int next(const TcPartition &part) {
+        const unsigned rbf = (c * u / cg) / kg;  // that CTA's first row block
+        const int slot = (int)((cs + c) * (unsigned)part.max_seg + (rb - rbf));
+        if (++c > cb && (int)(g + 1) < G) {
+            ++g;
+            enter_group(part);
+        }
+        return slot;
+    }
+};
+
+template <int T>
+__global__ void __launch_bounds__(kUnitRows, 8) tc_reduce_kernel(const StreamParams p, const TcPartition part) {
+    griddep_launch_dependents();
+    constexpr int kChunk = 32 / T;  // parts whose loads are in flight together
+    constexpr int kQ = T / 4;       // float4 per row of a part
+    TcPartCursor cur;
+    cur.rb = blockIdx.x;
+    cur.G = part.groups;
+    cur.KC = p.KC;
+    int np = 0;
+    for (cur.g = 0; (int)cur.g < cur.G; ++cur.g) {
+        cur.enter_group(part);
+        np += (int)cur.parts_in_group();
+    }
+    cur.g = 0;
+    cur.enter_group(part);
     // Every CTA waits for the GEMV, also those with nothing to sum: this grid
     // must not complete before the GEMV does, since the next kernel on the
     // stream (possibly the next call, reading Y) waits only for this one.
     griddep_wait();
     if (np <= 1) return;  // finished whole by the GEMV
-    const int r = threadIdx.x, row = (int)rb * kUnitRows + r;
-    const int nq = T / 4;  // float4 per row of a part
-    float4 a[4] = {};
-    for (int j0 = 0; j0 < np; j0 += kTcReduceChunk) {
-        float4 f[kTcReduceChunk][4];
-#pragma unroll
-        for (int j = 0; j < kTcReduceChunk; ++j) {
-            const float4 *src = reinterpret_cast<const float4 *>(
-                p.partials + (size_t)slots[j0 + j < np ? j0 + j : 0] * kTcPartialFloats + (size_t)r * T);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                f[j][q] = (j0 + j < np && q < nq) ? __ldcg(src + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int j = 0; j < kTcReduceChunk; ++j) {
-            if (j0 + j >= np) break;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (j0 + j == 0) {
-                    a[q] = f[j][q];  // parts are summed in CTA order starting from the first
-                } else {
-                    a[q].x += f[j][q].x; a[q].y += f[j][q].y; a[q].z += f[j][q].z; a[q].w += f[j][q].w;
-                }
-            }
-        }
-    }
+    const int r = threadIdx.x, row = (int)cur.rb * kUnitRows + r;
     float acc[16];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        acc[4 * q] = a[q].x; acc[4 * q + 1] = a[q].y; acc[4 * q + 2] = a[q].z; acc[4 * q + 3] = a[q].w;
+    for (int t = 0; t < 16; ++t) acc[t] = 0.f;
+    for (int j0 = 0; j0 < np; j0 += kChunk) {
+        float4 f[kChunk][kQ];
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+            if (j0 + j < np) {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    p.partials + (size_t)cur.next(part) * kTcPartialFloats + (size_t)r * T);
+#pragma unroll
+                for (int q = 0; q < kQ; ++q) f[j][q] = __ldcg(src + q);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+            if (j0 + j >= np) break;
+#pragma unroll
+            for (int q = 0; q < kQ; ++q) {
+                // parts are summed in CTA order; the first one replaces the zeros
+                const bool first = j0 + j == 0;
+                acc[4 * q] = first ? f[j][q].x : acc[4 * q] + f[j][q].x;
+                acc[4 * q + 1] = first ? f[j][q].y : acc[4 * q + 1] + f[j][q].y;
+                acc[4 * q + 2] = first ? f[j][q].z : acc[4 * q + 2] + f[j][q].z;
+                acc[4 * q + 3] = first ? f[j][q].w : acc[4 * q + 3] + f[j][q].w;
+            }
+        }
     }
     tc_store_row(p, acc, row, __ldg(p.gscale) * kTcXUnscale);
 }
@@ -731,7 +759,8 @@ cudaError_t launch_tc(const CUtensorMap &tw, const CUtensorMap &ts, const CUtens
     rc.stream = stream;
     rc.attrs = attr;
     rc.numAttrs = 1;
-    return cudaLaunchKernelEx(&rc, tc_reduce_kernel, p, part, T);
+    return T == 8 ? cudaLaunchKernelEx(&rc, tc_reduce_kernel<8>, p, part)
+                  : cudaLaunchKernelEx(&rc, tc_reduce_kernel<16>, p, part);
 }
 
 }  // namespace nvfp4
