@@ -27,7 +27,7 @@
 // past n zero-filled) and the epilogue warps convert it in place.  No
 // separate conversion kernel or X buffer in global memory.
 //
-// Warp roles (832 threads, one CTA per SM):
+// Warp roles (576 threads, one CTA per SM):
 //   warp 0       weight producer: 2D TMA loads of the unit's W tile
 //                (128B-swizzled) and scale tile into a ring of S stages.
 //   warp 1       X loads (see above).
@@ -40,12 +40,12 @@
 //                8 x tcgen05.mma.kind::f16 per half unit, M = 128 weight
 //                rows, N = 16 token columns, K = 16; A from tensor memory,
 //                B (= X) from shared memory.
-//   warps 6-21   dequantise: thread = weight row; warp (lane quarter q, k
-//                quarter j) turns rows 32q..32q+31, k 64j..64j+63 of every
+//   warps 6-13   dequantise: thread = weight row; warp (lane quarter q, k
+//                half j) turns rows 32q..32q+31, k 128j..128j+127 of every
 //                unit into f16 (E2M1 cvt times the E4M3 block scale: exact)
-//                and stores them with one tcgen05.st.  Each A buffer is
-//                handed over in two 128-k halves.
-//   warps 22-25  X conversion (bf16 -> f16 x 2^-8 in shared memory, unit by
+//                and stores them with two tcgen05.st of 32 columns; the four
+//                warps of a k half hand that half of the A buffer over.
+//   warps 14-17  X conversion (bf16 -> f16 x 2^-8 in shared memory, unit by
 //                unit in the order the CTA uses them), then the epilogue:
 //                per finished row-block segment, tcgen05.ld of the
 //                issuers' accumulators, summed in a fixed order, then either
@@ -92,10 +92,20 @@ constexpr int kTcWarpProducer = 0;
 constexpr int kTcWarpX = 1;
 constexpr int kTcWarpIssuer0 = kTcWarpX + 1;                    // issuers: warps 2 ..
 constexpr int kTcWarpDequant0 = kTcWarpIssuer0 + kTcIssuers;    // dequant: the next 16 warps
-constexpr int kTcDequantWarps = 16;
-constexpr int kTcWarpEpilogue0 = kTcWarpDequant0 + kTcDequantWarps;  // epilogue: warps 22..25
+// Eight dequant warps of 128 k each measured as fast as sixteen of 64 k at
+// n <= 4 and faster at n = 16, with fewer threads and registers to spare.
+constexpr int kTcDequantWarps = 8;
+constexpr int kTcDequantK = kTcUnitK * 4 / kTcDequantWarps;  // k of a unit per dequant warp (4 lane quarters)
+constexpr int kTcDqChunks = kTcDequantK / 32;                // 16-byte chunks of packed codes per lane
+constexpr int kTcDqStores = kTcDequantK / 64;                // 32-column tensor-memory stores per unit
+constexpr int kTcWarpEpilogue0 = kTcWarpDequant0 + kTcDequantWarps;  // epilogue: warps 14..17
 constexpr int kTcEpilogueWarps = 4;
-constexpr int kTcThreads = (kTcWarpEpilogue0 + kTcEpilogueWarps) * 32;  // 832
+constexpr int kTcThreads = (kTcWarpEpilogue0 + kTcEpilogueWarps) * 32;  // 576
+// Registers: the GEMV keeps one 2 K-register warp of room on every SM
+// sub-partition (16 K registers each; warp w sits on sub-partition w % 4) for a
+// reduction CTA beside it.
+constexpr int kTcWarpsPerSmsp = (kTcThreads / 32 + 3) / 4;
+constexpr int kTcMaxRegs = ((16384 - 2048) / (32 * kTcWarpsPerSmsp)) & ~7;
 constexpr float kTcXScale = 1.0f / 256.0f;       // 2^-8 applied to X before the f16 cast
 constexpr float kTcXUnscale = 256.0f;
 constexpr unsigned kDevErrXRange = 8u;           // some |x| >= 65520 * 2^8
@@ -121,8 +131,8 @@ __host__ __device__ constexpr int tc_barrier_count(int S, int KG) {
 }
 // Weight stages requested before X: the rest of the ring is requested only
 // once the X warp has requested X, so that X does not queue behind a full
-// ring of weight traffic from this SM.
-constexpr int kTcStagesBeforeX = 2;
+// ring of weight traffic from this SM (0, 2, 4, 8 measured: 4 is best).
+constexpr int kTcStagesBeforeX = 4;
 constexpr int kTcXConverterWarps = kTcEpilogueWarps;  // the epilogue warps convert X before their epilogue work
 
 // Group g of `groups` k-groups over KC unit columns: first unit column and width.
@@ -213,8 +223,10 @@ int tc_smem_bytes(int stages, int T, int kg_max) {
 
 void tc_group_host(int g, int groups, int KC, int *kstart, int *kg) { tc_group(g, groups, KC, kstart, kg); }
 
+// At most kTcMaxRegs registers a thread, so that a reduction CTA can sit
+// beside the GEMV CTA (see the launch notes above).
 template <int T>  // staged tokens: 8 (n <= 8) or 16
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __maxnreg__(kTcMaxRegs)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
                    const __grid_constant__ CUtensorMap tmap_x, const StreamParams p, const TcPartition part) {
     static_assert(T == 8 || T == 16, "staged tokens");
@@ -511,17 +523,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else if (warp < kTcWarpEpilogue0) {
         // ------------------------------------------------------------ dequant
-        const int e = warp - kTcWarpDequant0;  // 0..15
+        const int e = warp - kTcWarpDequant0;  // 0 .. kTcDequantWarps - 1
         const int lq = warp & 3;               // tensor-memory lane quarter this warp may access
-        const int kq = e >> 2;                 // which 64-k quarter of the unit
-        const int part = kq / (4 / kTcAParts);  // this warp's part of every A buffer
+        const int kw = e >> 2;                 // which kTcDequantK-wide k slice of the unit
+        const int part = kw * kTcDequantK / (kTcUnitK / kTcAParts);  // this warp's part of every A buffer
         const int r = 32 * lq + lane;          // row within the unit
         const uint32_t lane_bits = (uint32_t)(32 * lq) << 16;
-        // this lane's 64 k of row r in stage 0: two swizzled 16-byte chunks of
-        // the packed row, and 4 scale bytes (4-byte aligned)
-        const uint32_t w_off0 = r * 128 + (uint32_t)(((2 * kq) ^ (r & 7)) << 4);
-        const uint32_t w_off1 = r * 128 + (uint32_t)(((2 * kq + 1) ^ (r & 7)) << 4);
-        const uint8_t *const s_row = base + (sS - sW) + r * 16 + kq * 4;
+        // this lane's kTcDequantK k of row r: kTcDqChunks swizzled 16-byte chunks
+        // of the packed row, and kTcDequantK / 16 scale bytes (4-byte aligned)
+        const uint32_t w_row = (uint32_t)r * 128, w_sw = (uint32_t)(r & 7);
+        const uint8_t *const s_row = base + (sS - sW) + r * 16 + kw * (kTcDequantK / 16);
         bool ok = true;
         int slot = 0, ab = 0;            // ring stage, A buffer (i % S, i % kTcABufs kept incrementally)
         uint32_t fpar = 0, apar = 1;     // parities to wait for: full[slot]; aempty[ab] from round 1 on
@@ -530,37 +541,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ok = false;
                 break;
             }
-            const uint32_t wst = sW + slot * kTcWBytes;
-            const uint4 w0 = lds128(wst + w_off0);
-            const uint4 w1 = lds128(wst + w_off1);
-            const uint32_t sv = *reinterpret_cast<const uint32_t *>(s_row + slot * kTcSBytes);
+            const uint32_t wst = sW + slot * kTcWBytes + w_row;
+            uint4 wv[kTcDqChunks];
+#pragma unroll
+            for (int j = 0; j < kTcDqChunks; ++j)
+                wv[j] = lds128(wst + ((((uint32_t)(kw * kTcDqChunks + j)) ^ w_sw) << 4));
+            uint32_t sv[kTcDqStores];
+#pragma unroll
+            for (int h = 0; h < kTcDqStores; ++h)
+                sv[h] = *reinterpret_cast<const uint32_t *>(s_row + slot * kTcSBytes + 4 * h);
             __syncwarp();
             if (lane == 0) mbar_arrive(sEmpty + 8 * slot);  // the weight stage may be refilled
             if (++slot == S) {
                 slot = 0;
                 fpar ^= 1u;
             }
-            const uint32_t s01 = e4m3x2_to_f16x2(sv), s23 = e4m3x2_to_f16x2(sv >> 16);
-            const uint32_t sc[4] = {dup_lo(s01), dup_hi(s01), dup_lo(s23), dup_hi(s23)};
             if (i >= kTcABufs &&
                 __any_sync(0xffffffffu, !mbar_wait_bounded(sAEmpty + 8 * (ab * kTcAParts + part), apar))) {
                 ok = false;
                 break;
             }
-            const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            uint32_t v[32];
+            tc::fence_after_sync();  // the tensor-memory stores below follow the MMAs that read this part
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                uint32_t f;
-                switch (q & 3) {
-                    case 0: f = e2m1x2_to_f16x2<0>(words[q >> 2]); break;
-                    case 1: f = e2m1x2_to_f16x2<1>(words[q >> 2]); break;
-                    case 2: f = e2m1x2_to_f16x2<2>(words[q >> 2]); break;
-                    default: f = e2m1x2_to_f16x2<3>(words[q >> 2]); break;
+            for (int h = 0; h < kTcDqStores; ++h) {  // 64 k (32 columns) per store
+                const uint32_t s01 = e4m3x2_to_f16x2(sv[h]), s23 = e4m3x2_to_f16x2(sv[h] >> 16);
+                const uint32_t sc[4] = {dup_lo(s01), dup_hi(s01), dup_lo(s23), dup_hi(s23)};
+                const uint32_t words[8] = {wv[2 * h].x, wv[2 * h].y, wv[2 * h].z, wv[2 * h].w,
+                                           wv[2 * h + 1].x, wv[2 * h + 1].y, wv[2 * h + 1].z, wv[2 * h + 1].w};
+                uint32_t v[32];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    uint32_t f;
+                    switch (q & 3) {
+                        case 0: f = e2m1x2_to_f16x2<0>(words[q >> 2]); break;
+                        case 1: f = e2m1x2_to_f16x2<1>(words[q >> 2]); break;
+                        case 2: f = e2m1x2_to_f16x2<2>(words[q >> 2]); break;
+                        default: f = e2m1x2_to_f16x2<3>(words[q >> 2]); break;
+                    }
+                    v[q] = hmul2_u32(f, sc[q >> 3]);  // column q holds k pair (2q, 2q+1); 8 columns per scale block
                 }
-                v[q] = hmul2_u32(f, sc[q >> 3]);  // column q holds k pair (2q, 2q+1); 8 columns per scale block
+                tc::st_32x32b_x32(tbase + lane_bits + ab * kTcAColsPerUnit + (kw * kTcDqStores + h) * 32, v);
             }
-            tc::st_32x32b_x32(tbase + lane_bits + ab * kTcAColsPerUnit + kq * 32, v);
             tc::wait_st();
             tc::fence_before_sync();
             __syncwarp();
