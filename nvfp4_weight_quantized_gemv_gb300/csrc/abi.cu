@@ -452,6 +452,7 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
         sp.x = x + (size_t)t0 * K;
         sp.y = y + (size_t)t0 * y_stride;
         sp.n = tn;
+        sp.w_keep = (t0 + tn < n) ? 1 : 0;  // the next pass re-reads W: from L2, not HBM
         sp.y_vec2 = (N % 2 == 0) && ((reinterpret_cast<uintptr_t>(sp.y) & 3u) == 0);
         if (plan.variant == kTc) {
             CUtensorMap tx;

@@ -101,11 +101,14 @@ constexpr int kTcDqStores = kTcDequantK / 64;                // 32-column tensor
 constexpr int kTcWarpEpilogue0 = kTcWarpDequant0 + kTcDequantWarps;  // epilogue: warps 14..17
 constexpr int kTcEpilogueWarps = 4;
 constexpr int kTcThreads = (kTcWarpEpilogue0 + kTcEpilogueWarps) * 32;  // 576
-// Registers: the GEMV keeps one 2 K-register warp of room on every SM
-// sub-partition (16 K registers each; warp w sits on sub-partition w % 4) for a
-// reduction CTA beside it.
+// Registers: the GEMV keeps room for one warp of the reduction kernel (at
+// most kTcReduceRegs registers a thread) on every SM sub-partition (16 K
+// registers each; warp w sits on sub-partition w % 4), so that a reduction CTA
+// fits beside it.
+constexpr int kTcReduceRegs = 96;
 constexpr int kTcWarpsPerSmsp = (kTcThreads / 32 + 3) / 4;
-constexpr int kTcMaxRegs = ((16384 - 2048) / (32 * kTcWarpsPerSmsp)) & ~7;
+constexpr int kTcMaxRegs = ((16384 - 32 * kTcReduceRegs) / (32 * kTcWarpsPerSmsp)) & ~7;
+static_assert(kTcMaxRegs >= 64, "register budget");
 constexpr float kTcXScale = 1.0f / 256.0f;       // 2^-8 applied to X before the f16 cast
 constexpr float kTcXUnscale = 256.0f;
 constexpr unsigned kDevErrXRange = 8u;           // some |x| >= 65520 * 2^8
@@ -281,7 +284,10 @@ __global__ void __maxnreg__(kTcMaxRegs)
     // The weight stream starts first: the producer thread sets up the ring's
     // barriers and requests the first stages before anything else (the ring is
     // touched by no other thread before the CTA barrier below).
-    const uint64_t w_policy = l2_policy_evict_first();
+    // Weights are read once per call: streamed with evict-first, except in a
+    // pass that another pass over the same weights follows (n > 16), which
+    // leaves them in L2 (evict-last) so that the next pass does not read HBM.
+    const uint64_t w_policy = p.w_keep ? l2_policy_evict_last() : l2_policy_evict_first();
     int w_rb = rb0, w_kl = kl0, issued = 0;
     auto issue_w = [&](int i) {
         const int slot = i % S;
@@ -666,10 +672,10 @@ __global__ void __maxnreg__(kTcMaxRegs)
 // row block rb are the unit ranges of CTAs [ca, cb] of every k-group, taken
 // in CTA order; part (CTA c) sits in c's slot for rb (c's partial tiles are
 // indexed by row block from its first one).  Each thread walks that list
-// itself and fetches its row of 32 / T parts at a time into registers (all
+// itself and fetches its row of 64 / T parts at a time into registers (all
 // those loads in flight together: one memory round trip per chunk), then sums
-// them in order.  No shared memory and at most 64 registers a thread, so a
-// reduction CTA fits on an SM next to a GEMV CTA: it can be resident (and
+// them in order.  No shared memory and at most kTcReduceRegs registers a
+// thread, so a reduction CTA fits on an SM next to a GEMV CTA: it can be resident (and
 // waiting) before the GEMV finishes, and it never keeps the next call's GEMV
 // CTA off an SM.  Row blocks finished whole by the GEMV (a single part) are
 // skipped.  Index arithmetic is 32-bit: the planner keeps row_blocks * KC *
@@ -701,9 +707,9 @@ struct TcPartCursor {  // walks the parts of one row block in (group, CTA) order
 };
 
 template <int T>
-__global__ void __launch_bounds__(kUnitRows, 8) tc_reduce_kernel(const StreamParams p, const TcPartition part) {
+__global__ void __maxnreg__(kTcReduceRegs) tc_reduce_kernel(const StreamParams p, const TcPartition part) {
     griddep_launch_dependents();
-    constexpr int kChunk = 32 / T;  // parts whose loads are in flight together
+    constexpr int kChunk = 64 / T;  // parts whose loads are in flight together
     constexpr int kQ = T / 4;       // float4 per row of a part
     TcPartCursor cur;
     cur.rb = blockIdx.x;

@@ -38,6 +38,7 @@ struct StreamParams {
     int stages;
     int y_vec2;          // bf16x2 stores allowed (N even and y 4-byte aligned)
     int swiglu;          // tcgen05 only: rows 2f, 2f+1 are gate_f, up_f; y is h[n][N/2] = silu(gate) * up
+    int w_keep;          // tcgen05 only: another pass over the same weights follows (keep them in L2)
 };
 
 // Grouped read-once GEMV over routed experts (moe_gemv.cu).
