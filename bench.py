@@ -550,8 +550,12 @@ def main():
 
     plan = nv.nvfp4_gemv_plan(calls[-1][1], *SHAPES[calls[-1][0]], variant=variant, tiling=tiling)
     def launches(plan_info):
-        # tcgen05 path: GEMV and split-row reduction per pass
-        return plan_info["passes"] * (2 if plan_info["variant"] == "tc" else 1)
+        # tcgen05 path: GEMV and split-row reduction per pass, plus the X
+        # conversion when a pass stages 32 tokens (n > 16)
+        if plan_info["variant"] != "tc":
+            return plan_info["passes"]
+        wide = max(plan_info["tile_tokens"]) > 16
+        return plan_info["passes"] * (3 if wide else 2)
 
     launches_per_step = sum(launches(nv.nvfp4_gemv_plan(n, *SHAPES[s], variant=variant, tiling=tiling))
                             for s, n in calls)

@@ -79,7 +79,9 @@ typedef struct nvfp4_gemv_opts {
     int num_ctas;            /* 0 = one CTA per SM; else 1..#SMs (persistent grid size) */
     int stages;              /* 0 = as many TMA ring stages as shared memory allows; else 2..8 */
     void *workspace;         /* NULL = library-owned per-stream workspace; else device memory */
-    size_t workspace_bytes;  /* size of `workspace` (see nvfp4_gemv_workspace_size) */
+    size_t workspace_bytes;  /* size of `workspace` (see nvfp4_gemv_workspace_size); if nonzero (with or without
+                                `workspace`) the plan keeps its scratch within it: n > 16 then takes 16-token
+                                passes instead of 32-token ones when those need more */
 } nvfp4_gemv_opts;
 
 /* Launch plan the library would use (for tests and benchmarks). */

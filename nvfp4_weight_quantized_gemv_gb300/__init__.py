@@ -243,9 +243,10 @@ def nvfp4_gemv_workspace_size(n, N, K, variant=0, tiling=0, num_ctas=0, stages=0
     return b.value
 
 
-def nvfp4_gemv_plan(n, N, K, variant=0, tiling=0, num_ctas=0, stages=0) -> dict:
+def nvfp4_gemv_plan(n, N, K, variant=0, tiling=0, num_ctas=0, stages=0, workspace_bytes=0) -> dict:
     info = nvfp4_gemv_plan_info()
     o = _opts(variant, tiling, num_ctas, stages)
+    o.workspace_bytes = int(workspace_bytes)  # a declared scratch size caps the plan
     _check(lib().nvfp4_gemv_plan(n, N, K, ctypes.byref(o), ctypes.byref(info)))
     return dict(variant=VARIANT_NAMES[info.variant], tiling=TILING_NAMES[info.tiling], passes=info.passes,
                 tile_tokens=list(info.tile_tokens[:min(info.passes, 16)]), num_ctas=info.num_ctas,

@@ -163,14 +163,15 @@ static nvfp4_status encode_2d(CUtensorMap *map, const void *ptr, uint64_t cols, 
 // 128-byte-swizzled K-major layout; tokens past n read as zeros.  The kernel
 // converts the landed box to f16 in place.  (With 8 staged tokens the kernel
 // copies X rows itself and needs no map.)
-static nvfp4_status encode_x(CUtensorMap *map, const uint16_t *x, int n, int K) {
+static nvfp4_status encode_x(CUtensorMap *map, const uint16_t *x, int n, int K, int box_tokens = 16) {
     EncodeTiledFn fn;
     nvfp4_status st = get_encode_fn(&fn);
     if (st != NVFP4_OK) return st;
     const cuuint64_t dims[3] = {64, (cuuint64_t)n, (cuuint64_t)K / 64};
     const cuuint64_t strides[2] = {(cuuint64_t)K * 2, 128};
-    const cuuint32_t box[3] = {64, 16, 4};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_tokens, 4};
     const cuuint32_t estr[3] = {1, 1, 1};
+    // a 2-byte element type either way: the copy does not convert (T = 32 maps the f16 X)
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(x), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -187,7 +188,8 @@ struct Plan {
     int stages = 0;
     int smem = 0;
     long long units = 0;
-    int tc_tokens = 0;  // tcgen05 kernel: tokens staged per pass (8 or 16)
+    int tc_tokens = 0;  // tcgen05 kernel: tokens staged per pass (8, 16 or 32)
+    size_t partial_bytes = 0, x16_bytes = 0;
     TcPartition part{};  // tcgen05 kernel: k-groups and their CTAs
     size_t counter_bytes = 0, ws_bytes = 0;
 };
@@ -280,8 +282,22 @@ static std::vector<int> greedy_321(int n) {
     return t;
 }
 
+static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nvfp4_gemv_opts &o, int sms,
+                                     int smem_optin, int tc_per_pass, Plan *plan);
+
+// The tcgen05 kernel takes up to 32 tokens per pass (n = 17..32 in one read of
+// W); when the caller declares a scratch size (workspace_bytes) too small for
+// the 32-token pass, it gets 16-token passes instead.
 static nvfp4_status make_plan(int n, int N, int K, bool fast_ok, const nvfp4_gemv_opts &o, int sms, int smem_optin,
                               Plan *plan) {
+    nvfp4_status st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kTcMaxTokensPerPass, plan);
+    if (st == NVFP4_OK && plan->tc_tokens == 32 && o.workspace_bytes != 0 && o.workspace_bytes < plan->ws_bytes)
+        st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kMaxTokensPerPass, plan);
+    return st;
+}
+
+static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nvfp4_gemv_opts &o, int sms,
+                                     int smem_optin, int tc_per_pass, Plan *plan) {
     Plan p;
     p.variant = o.variant;
     const bool tc_ok = fast_ok;
@@ -295,14 +311,14 @@ static nvfp4_status make_plan(int n, int N, int K, bool fast_ok, const nvfp4_gem
                     "the tcgen05 variant needs K %% 256 == 0 and 16-byte aligned w_packed, w_scale_e4m3 and x_bf16");
     p.tiling = (o.tiling == NVFP4_TILING_AUTO) ? NVFP4_TILING_ONE_PASS : o.tiling;
 
-    int per_pass = kMaxTokensPerPass;
+    int per_pass = p.variant == kTc ? tc_per_pass : kMaxTokensPerPass;
     if (p.variant == kMma || p.variant == kSimt) {
         // largest token count whose X still leaves room for two ring stages
         const int room = smem_optin - stream_smem_bytes(2, 0, K);
         int fit = room / (2 * K);
         if (fit < 1) return fail(NVFP4_ERR_UNSUPPORTED, "K = %d too large for the streaming kernel", K);
         per_pass = fit < per_pass ? fit : per_pass;
-    }  // tcgen05: 16 tokens per pass for any K (X is held per k-group)
+    }  // tcgen05: 16 (X held per k-group) or 32 (X streamed per unit) tokens per pass for any K
     if (p.tiling == NVFP4_TILING_GREEDY_321) {
         p.tiles = greedy_321(n);
     } else {
@@ -311,7 +327,7 @@ static nvfp4_status make_plan(int n, int N, int K, bool fast_ok, const nvfp4_gem
     if (p.variant != kGeneric) {
         int max_tile = 0;
         for (int t : p.tiles) max_tile = t > max_tile ? t : max_tile;
-        const int T = max_tile > 8 ? 16 : 8;
+        const int T = max_tile > 16 ? 32 : max_tile > 8 ? 16 : 8;
         const int unit_k = p.variant == kTc ? kTcUnitKHost : kUnitK;
         p.units = (long long)((N + kUnitRows - 1) / kUnitRows) * (K / unit_k);
         int ctas = o.num_ctas ? o.num_ctas : sms;
@@ -343,9 +359,11 @@ static nvfp4_status make_plan(int n, int N, int K, bool fast_ok, const nvfp4_gem
         p.smem = smem_for(stages);
         p.tc_tokens = p.variant == kTc ? T : 0;
         p.counter_bytes = ws_counter_bytes(sms, (N + kUnitRows - 1) / kUnitRows);
-        p.ws_bytes = p.counter_bytes + (p.variant == kTc ? (size_t)ctas * p.part.max_seg * kConsumerWarps *
-                                                                   kSlotFloats * sizeof(float)
-                                                         : stream_partial_bytes(sms));
+        p.partial_bytes = p.variant == kTc ? (size_t)ctas * p.part.max_seg * tc_partial_floats(T) * sizeof(float)
+                                           : stream_partial_bytes(sms);
+        // T = 32: the pass's X as f16 x 2^-8 follows the partial tiles (256-byte aligned)
+        p.x16_bytes = (p.variant == kTc && T == 32) ? (size_t)32 * K * 2 : 0;
+        p.ws_bytes = p.counter_bytes + ((p.partial_bytes + 255) & ~(size_t)255) + p.x16_bytes;
     }
     *plan = p;
     return NVFP4_OK;
@@ -438,6 +456,8 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
     sp.gscale = gs;
     sp.counters = static_cast<unsigned *>(work);
     sp.partials = reinterpret_cast<float *>(static_cast<char *>(work) + plan.counter_bytes);
+    uint16_t *const x16 = reinterpret_cast<uint16_t *>(static_cast<char *>(work) + plan.counter_bytes +
+                                                       ((plan.partial_bytes + 255) & ~(size_t)255));
     sp.err = d->err_word;
     sp.units = plan.units;
     sp.ctas = plan.ctas;
@@ -458,6 +478,12 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
             CUtensorMap tx;
             memset(&tx, 0, sizeof tx);
             if (plan.tc_tokens == 16 && (st = encode_x(&tx, sp.x, tn, K)) != NVFP4_OK) return st;
+            if (plan.tc_tokens == 32) {
+                // the pass's X converted once to f16 x 2^-8; the GEMV streams it per unit
+                if ((e = launch_tc_x16(sp.x, x16, tn, K, d->err_word, stream)) != cudaSuccess)
+                    return cuda_fail(e, "X conversion kernel launch");
+                if ((st = encode_x(&tx, x16, tn, K, 32)) != NVFP4_OK) return st;
+            }
             e = launch_tc(tw, ts, tx, sp, plan.part, plan.tc_tokens, plan.smem, stream);
         } else {
             e = launch_stream(plan.variant, tw, ts, sp, plan.smem, stream);

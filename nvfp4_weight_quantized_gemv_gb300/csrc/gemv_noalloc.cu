@@ -71,7 +71,10 @@ extern "C" nvfp4_status nvfp4_gemv_batched_noalloc(const uint8_t *w_packed, cons
     if (dev < 0 || dev >= kMaxDevices)
         return noalloc_fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_gemv_batched_noalloc: device ordinal too large");
     size_t counter_bytes = 0, needed = 0;
-    const int st = workspace_layout(n, N, K, nullptr, &counter_bytes, &needed);
+    nvfp4_gemv_opts cap;  // plan within the static scratch (32-token passes fall back to 16 if it is too small)
+    std::memset(&cap, 0, sizeof cap);
+    cap.workspace_bytes = kNoAllocScratchBytes;
+    const int st = workspace_layout(n, N, K, &cap, &counter_bytes, &needed);
     if (st != NVFP4_OK) return (nvfp4_status)st;
     if (needed > kNoAllocScratchBytes) {
         char buf[256];

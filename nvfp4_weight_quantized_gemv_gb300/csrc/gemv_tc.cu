@@ -113,9 +113,15 @@ constexpr float kTcXScale = 1.0f / 256.0f;       // 2^-8 applied to X before the
 constexpr float kTcXUnscale = 256.0f;
 constexpr unsigned kDevErrXRange = 8u;           // some |x| >= 65520 * 2^8
 constexpr unsigned kDevErrSmemBase = 64u;        // dynamic shared memory not 1024-byte aligned
-constexpr int kTcPartialFloats = kConsumerWarps * kSlotFloats;  // one partial tile slot: 128 rows x 16 tokens
+// 32 staged tokens (n = 17..32): X is not resident but streamed per unit
+// through a ring of kTcXRing slots, already converted to f16 x 2^-8 by
+// tc_x16_kernel (the k-group partition stays that of n <= 16, so results do
+// not depend on n).
+constexpr int kTcXRing = 4;
+// x-barrier slots: one per unit column of the group (T <= 16) or ring slot (T = 32)
+__host__ __device__ constexpr int tc_xbars(int KG) { return KG > kTcXRing ? KG : kTcXRing; }
 
-static_assert(kTcDCol + kTcIssuers * 2 * 16 <= (int)kTcTmemCols, "tensor memory");
+static_assert(kTcDCol + kTcIssuers * 2 * 32 <= (int)kTcTmemCols, "tensor memory (up to 32 token columns)");
 
 // Each A buffer is handed from the dequant warps to its issuer, and back, in
 // kTcAParts parts of 256 / kTcAParts k (the lane-quarter warps of those k
@@ -127,10 +133,10 @@ constexpr int kTcStepsPerPart = 16 / kTcAParts;  // MMA k-steps (16 k each) per 
 constexpr int kTcPartsPerIssuer = kTcAParts / kTcIssuersPerBuf;
 static_assert(kTcPartsPerIssuer * kTcIssuersPerBuf == kTcAParts, "issuers split a buffer's parts evenly");
 
-// barriers: full[S] empty[S] xloaded[KG] xfull[KG] afull[B][P] aempty[B][P] dfull[I][2] dempty[2] final[I] xreq
-// (B A buffers, P parts, I issuers)
+// barriers: full[S] empty[S] xloaded[XB] xfull[XB] afull[B][P] aempty[B][P] dfull[I][2] dempty[2] final[I] xreq
+// (B A buffers, P parts, I issuers, XB = tc_xbars(KG))
 __host__ __device__ constexpr int tc_barrier_count(int S, int KG) {
-    return 2 * S + 2 * KG + 2 * kTcABufs * kTcAParts + 2 * kTcIssuers + 2 + kTcIssuers + 1;
+    return 2 * S + 2 * tc_xbars(KG) + 2 * kTcABufs * kTcAParts + 2 * kTcIssuers + 2 + kTcIssuers + 1;
 }
 // Weight stages requested before X: the rest of the ring is requested only
 // once the X warp has requested X, so that X does not queue behind a full
@@ -170,14 +176,17 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 // of a pair sit in lanes 2i and 2i + 1 of the calling warp, and the even lane
 // stores h[t][f] = bf16(silu(gate) * up), silu(a) = a / (1 + exp(-a)), in fp32.
 // Every lane of the warp must call it (the pair exchange is a shuffle).
-__device__ __forceinline__ void tc_store_row(const StreamParams &p, const float (&v)[16], int row, float gs) {
+// v[j] is token t0 + j.
+__device__ __forceinline__ void tc_store_row(const StreamParams &p, const float (&v)[16], int row, float gs,
+                                             int t0 = 0) {
     const int lane = threadIdx.x & 31;
     if (!p.swiglu) {
         if (row < p.N) {
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
+            for (int j = 0; j < 16; ++j) {
+                const int t = t0 + j;
                 if (t < p.n) {
-                    __nv_bfloat16 hv = __float2bfloat16_rn(v[t] * gs);
+                    __nv_bfloat16 hv = __float2bfloat16_rn(v[j] * gs);
                     p.y[(size_t)t * p.N + row] = *reinterpret_cast<uint16_t *>(&hv);
                 }
             }
@@ -186,8 +195,9 @@ __device__ __forceinline__ void tc_store_row(const StreamParams &p, const float 
     }
     const int F = p.N >> 1;
 #pragma unroll
-    for (int t = 0; t < 16; ++t) {
-        const float a = v[t] * gs;
+    for (int j = 0; j < 16; ++j) {
+        const int t = t0 + j;
+        const float a = v[j] * gs;
         const float up = __shfl_down_sync(0xffffffffu, a, 1);
         if (t < p.n && (lane & 1) == 0 && row < p.N) {
             const float h = a / (1.0f + expf(-a)) * up;
@@ -215,24 +225,30 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, uint32_t 
 
 // X area: kg_max units x 16 token rows x 512 B -- the f16 X for T = 16, or
 // the f16 X (8 rows) plus the bf16 staging (8 rows) for T = 8: the same size,
-// so the plan does not depend on n.
+// so the partition does not depend on n; for T = 32, kTcXRing slots of 32
+// token rows x 512 B.
 // The dynamic shared memory starts 1024-byte aligned (the kernel checks it),
 // so no alignment slack is reserved: the GEMV then leaves room on its SM for a
 // reduction CTA (its 1 KB of reserved shared memory).
+__host__ __device__ inline int tc_xarea_bytes(int T, int kg_max) {
+    return T == 32 ? kTcXRing * 32 * 512 : kg_max * 16 * 512;
+}
 int tc_smem_bytes(int stages, int T, int kg_max) {
-    (void)T;
-    return stages * (kTcWBytes + kTcSBytes) + kg_max * 16 * 512 + 1024 + 8 * tc_barrier_count(stages, kg_max) + 64;
+    return stages * (kTcWBytes + kTcSBytes) + tc_xarea_bytes(T, kg_max) + 1024 + 8 * tc_barrier_count(stages, kg_max) +
+           64;
 }
 
 void tc_group_host(int g, int groups, int KC, int *kstart, int *kg) { tc_group(g, groups, KC, kstart, kg); }
 
 // At most kTcMaxRegs registers a thread, so that a reduction CTA can sit
 // beside the GEMV CTA (see the launch notes above).
-template <int T>  // staged tokens: 8 (n <= 8) or 16
+template <int T>  // staged tokens: 8 (n <= 8), 16 (n <= 16) or 32 (X ring, pre-converted)
 __global__ void __maxnreg__(kTcMaxRegs)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
                    const __grid_constant__ CUtensorMap tmap_x, const StreamParams p, const TcPartition part) {
-    static_assert(T == 8 || T == 16, "staged tokens");
+    static_assert(T == 8 || T == 16 || T == 32, "staged tokens");
+    constexpr bool kRing = T == 32;        // X streamed per unit through kTcXRing slots
+    constexpr int kAcc = T < 16 ? 16 : T;  // accumulator columns per (issuer, segment buffer)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t sW = smem_u32(smem_raw);
     if (sW & 1023u) {  // the swizzled tiles need a 1024-byte aligned base; never expected
@@ -260,17 +276,20 @@ __global__ void __maxnreg__(kTcMaxRegs)
     const int nx = count < kg ? count : kg;              // X units this CTA uses
 
     constexpr uint32_t xslot = (uint32_t)T * 512;       // one unit's X: 4 boxes of T tokens x 64 k (128 B rows)
+    const int xb = tc_xbars(kg_max);                     // x-barrier slots
     constexpr uint32_t xbox = (uint32_t)T * 128;
     const uint32_t sS = sW + S * kTcWBytes;
     const uint32_t sX = sS + S * kTcSBytes;             // X of the group [kg_max units], 1024-byte aligned
     const uint32_t sStage = sX + kg_max * xslot;        // T = 8: bf16 rows [8 tokens][kg_max * 256 k]
     const uint32_t stage_pitch = (uint32_t)kg_max * 512; // bytes per staged token row
-    const uint32_t sZero = sX + kg_max * 16 * 512;      // 1024 zero bytes (one swizzle atom)
+    const uint32_t sZero = sX + tc_xarea_bytes(T, kg_max);  // 1024 zero bytes (one swizzle atom)
     const uint32_t sFull = sZero + 1024;                // W + scales of a stage landed
     const uint32_t sEmpty = sFull + 8 * S;              // dequant warps done with W + scales, count 16
-    const uint32_t sXLoaded = sEmpty + 8 * S;           // [unit column] bf16 X landed (TMA), one phase
-    const uint32_t sXFull = sXLoaded + 8 * kg_max;      // [unit column] f16 X ready, count 5 (converter warps)
-    const uint32_t sAFull = sXFull + 8 * kg_max;        // [buffer][part], count = warps per part
+    // T <= 16: [unit column] X landed (TMA, one phase) / f16 X ready (converter warps);
+    // T = 32: [ring slot] X landed (TMA) / slot free (commits of the unit's issuers)
+    const uint32_t sXLoaded = sEmpty + 8 * S;
+    const uint32_t sXFull = sXLoaded + 8 * xb;
+    const uint32_t sAFull = sXFull + 8 * xb;            // [buffer][part], count = warps per part
     const uint32_t sAEmpty = sAFull + 8 * kTcABufs * kTcAParts;   // [buffer][part], count 1 (commit)
     const uint32_t sDFull = sAEmpty + 8 * kTcABufs * kTcAParts;   // [issuer][segment buffer], count 1 (commit)
     const uint32_t sDEmpty = sDFull + 16 * kTcIssuers;  // [segment buffer], count 4 (epilogue warps)
@@ -309,9 +328,9 @@ __global__ void __maxnreg__(kTcMaxRegs)
         fence_barrier_init();
         const int pre = count < kTcStagesBeforeX ? count : (kTcStagesBeforeX < S ? kTcStagesBeforeX : S);
         for (; issued < pre; ++issued) issue_w(issued);
-        for (int s = 0; s < kg_max; ++s) {
+        for (int s = 0; s < xb; ++s) {
             mbar_init(sXLoaded + 8 * s, 1);
-            mbar_init(sXFull + 8 * s, kTcXConverterWarps);
+            mbar_init(sXFull + 8 * s, kRing ? kTcIssuersPerBuf : kTcXConverterWarps);
         }
         for (int b = 0; b < kTcABufs * kTcAParts; ++b) {
             mbar_init(sAFull + 8 * b, kTcDequantWarps / kTcAParts);
@@ -323,7 +342,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
         mbar_init(sXReq, 1);
         fence_barrier_init();
     }
-    if (T == 16 && warp == kTcWarpX && lane == 0) prefetch_tensormap(&tmap_x);  // T = 8 uses no X map
+    if (T >= 16 && warp == kTcWarpX && lane == 0) prefetch_tensormap(&tmap_x);  // T = 8 uses no X map
     if (warp == kTcWarpIssuer0) {
         tc::tmem_alloc(sMisc, kTcTmemCols);
         tc::tmem_relinquish();
@@ -428,7 +447,33 @@ __global__ void __maxnreg__(kTcMaxRegs)
         // ------------------------------------------------------------------- X
         // The unit in column l of the group sits at sX + l * xslot.
         griddep_wait();  // X may be the output of the kernel ahead of this one
-        if (lane == 0) {
+        if (kRing && lane == 0) {
+            // unit i's X (its unit column of the group) into ring slot i % kTcXRing,
+            // once both issuers of the slot's previous unit have committed
+            const uint64_t policy = l2_policy_evict_last();  // every CTA of the group reads the same X
+            const int first = count < kTcXRing ? count : kTcXRing;
+            int loaded = 0;
+            for (; loaded < count; ++loaded) {
+                const int slot = loaded % kTcXRing;
+                if (loaded >= kTcXRing &&
+                    !mbar_wait_bounded(sXFull + 8 * slot, ((loaded / kTcXRing) - 1) & 1)) {
+                    atomicOr(p.err, kDevErrTimeoutEmpty);
+                    break;
+                }
+                const int l = (kl0 + loaded) % kg;
+                mbar_arrive_expect_tx(sXLoaded + 8 * slot, xslot);
+                tma_load_3d(sX + slot * xslot, &tmap_x, 0, 0, (kstart + l) * 4, sXLoaded + 8 * slot, policy);
+                if (loaded == first - 1) mbar_arrive(sXReq);  // the producer may request the rest of its ring
+            }
+            if (loaded < first) mbar_arrive(sXReq);
+            // wait (bounded) for the copies in flight before the warp leaves
+            for (int i = loaded > kTcXRing ? loaded - kTcXRing : 0; i < loaded; ++i) {
+                if (!mbar_wait_bounded(sXLoaded + 8 * (i % kTcXRing), (i / kTcXRing) & 1)) {
+                    atomicOr(p.err, kDevErrTimeoutDrain);
+                    break;
+                }
+            }
+        } else if (lane == 0) {
             const uint64_t policy = l2_policy_evict_last();  // every CTA of the group reads the same X
             if (T == 8) {
                 // one bulk copy per token: its kg units of the group, contiguous in X
@@ -463,7 +508,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
         const int a = w / kTcIssuersPerBuf;   // its A buffer: units i with i % kTcABufs == a
         const int p0 = (w % kTcIssuersPerBuf) * kTcPartsPerIssuer;  // its parts of each unit
         if (lane == 0) {
-            const uint32_t idesc = tc::idesc_f16_f32(kUnitRows, 16);
+            const uint32_t idesc = tc::idesc_f16_f32(kUnitRows, kAcc);
             bool ok = true;
             int seg = 0, kl = kl0;
             for (int i = 0; i < count && ok; ++seg) {
@@ -475,16 +520,18 @@ __global__ void __maxnreg__(kTcMaxRegs)
                     ok = false;
                     break;
                 }
-                const uint32_t d_tmem = tbase + kTcDCol + w * 32 + sb * 16;
+                const uint32_t d_tmem = tbase + kTcDCol + w * 2 * kAcc + sb * kAcc;
                 bool first = true;
                 int ib = i + ((a - i % kTcABufs) + kTcABufs) % kTcABufs;  // first unit of this issuer
                 for (; ib <= iend; ib += kTcABufs) {
                     const int l = kl + (ib - i);  // unit column within the group
-                    if (!mbar_wait_bounded(sXFull + 8 * l, 0)) {
+                    const int xs = ib % kTcXRing;  // T = 32: ring slot of unit ib
+                    if (kRing ? !mbar_wait_bounded(sXLoaded + 8 * xs, (ib / kTcXRing) & 1)
+                              : !mbar_wait_bounded(sXFull + 8 * l, 0)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t xbase = sX + l * xslot;
+                    const uint32_t xbase = kRing ? sX + xs * xslot : sX + l * xslot;
                     const uint32_t a_tmem = tbase + a * kTcAColsPerUnit;
                     const unsigned par = (ib / kTcABufs) & 1;
 #pragma unroll
@@ -496,7 +543,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
 #pragma unroll
                         for (int h = 0; h < kBoxes; ++h) {
                             const uint32_t box = xbase + (uint32_t)(part * kBoxes + h) * xbox;
-                            bd[h] = tc::smem_desc_sw128(box, (T == 16) ? 1024u : (sZero - box));
+                            bd[h] = tc::smem_desc_sw128(box, (T >= 16) ? 1024u : (sZero - box));
                         }
                         if (!mbar_wait_bounded(sAFull + 8 * (a * kTcAParts + part), par)) {
                             ok = false;
@@ -515,6 +562,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
                         tc::commit(sAEmpty + 8 * (a * kTcAParts + part));
                     }
                     if (!ok) break;
+                    if (kRing) tc::commit(sXFull + 8 * xs);  // the X slot may be refilled once these MMAs are done
                     first = false;
                 }
                 // every issuer closes every segment, so the epilogue sees each phase
@@ -623,36 +671,41 @@ __global__ void __maxnreg__(kTcMaxRegs)
             }
             tc::fence_after_sync();
             const int len = iend - i + 1;
-            float v[16];
-            bool have = false;
-#pragma unroll
-            for (int q = 0; q < kTcIssuers; ++q) {  // fixed order: issuer 0, 1, ...
-                const int qb = q / kTcIssuersPerBuf;  // the A buffer (unit residue) of issuer q
-                const bool contributed = len >= kTcABufs || ((qb - i % kTcABufs + kTcABufs) % kTcABufs) < len;
-                if (!contributed) continue;
-                uint32_t d[16];
-                tc::ld_32x32b_x16(tbase + lane_bits + kTcDCol + q * 32 + sb * 16, d);
-                tc::wait_ld();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = have ? v[j] + __uint_as_float(d[j]) : __uint_as_float(d[j]);
-                have = true;
-            }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sDEmpty + 8 * sb);
-
             const int row = rb * kUnitRows + 32 * lq + lane;
-            if (G == 1 && kfirst == 0 && klast == kg - 1) {
-                tc_store_row(p, v, row, gs);  // the whole row block is this segment: finish it here
-            } else {
-                // one part of a split row block: publish the fp32 tile (T tokens per row);
-                // the reduction kernel that follows sums the parts in CTA order
-                float4 *mine = reinterpret_cast<float4 *>(
-                    p.partials + ((size_t)blockIdx.x * part.max_seg + (rb - rb0)) * kTcPartialFloats +
-                    (size_t)(32 * lq + lane) * T);
+            const bool whole = G == 1 && kfirst == 0 && klast == kg - 1;
+            float *const mine = p.partials + ((size_t)blockIdx.x * part.max_seg + (rb - rb0)) * tc_partial_floats(T) +
+                                (size_t)(32 * lq + lane) * T;
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if (q < T / 4) __stcg(mine + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+            for (int c = 0; c < kAcc / 16; ++c) {  // 16 token columns at a time
+                float v[16];
+                bool have = false;
+#pragma unroll
+                for (int q = 0; q < kTcIssuers; ++q) {  // fixed order: issuer 0, 1, ...
+                    const int qb = q / kTcIssuersPerBuf;  // the A buffer (unit residue) of issuer q
+                    const bool contributed = len >= kTcABufs || ((qb - i % kTcABufs + kTcABufs) % kTcABufs) < len;
+                    if (!contributed) continue;
+                    uint32_t d[16];
+                    tc::ld_32x32b_x16(tbase + lane_bits + kTcDCol + q * 2 * kAcc + sb * kAcc + c * 16, d);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = have ? v[j] + __uint_as_float(d[j]) : __uint_as_float(d[j]);
+                    have = true;
+                }
+                if (c == kAcc / 16 - 1) {  // every accumulator column of the segment is read
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sDEmpty + 8 * sb);
+                }
+                if (whole) {
+                    tc_store_row(p, v, row, gs, 16 * c);  // the whole row block is this segment: finish it here
+                } else {
+                    // one part of a split row block: publish the fp32 tile (T tokens per row);
+                    // the reduction kernel that follows sums the parts in CTA order
+                    float4 *const dst = reinterpret_cast<float4 *>(mine + 16 * c);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (q < T / 4) __stcg(dst + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+                }
             }
             i = iend + 1;
             kl = 0;
@@ -706,28 +759,16 @@ struct TcPartCursor {  // walks the parts of one row block in (group, CTA) order
     }
 };
 
-template <int T>
-__global__ void __maxnreg__(kTcReduceRegs) tc_reduce_kernel(const StreamParams p, const TcPartition part) {
-    griddep_launch_dependents();
-    constexpr int kChunk = 64 / T;  // parts whose loads are in flight together
-    constexpr int kQ = T / 4;       // float4 per row of a part
-    TcPartCursor cur;
-    cur.rb = blockIdx.x;
-    cur.G = part.groups;
-    cur.KC = p.KC;
-    int np = 0;
-    for (cur.g = 0; (int)cur.g < cur.G; ++cur.g) {
-        cur.enter_group(part);
-        np += (int)cur.parts_in_group();
-    }
+// One sweep of the reduction over a row block's parts: tokens h*TT .. h*TT+TT-1
+// of this thread's row, 64 / TT parts' loads in flight at a time, summed in
+// part order (CTA order, group-major), then stored.
+template <int T, int TT>
+__device__ __forceinline__ void tc_reduce_sweep(const StreamParams &p, const TcPartition &part, TcPartCursor cur,
+                                                int np, int r, int row, int h) {
+    constexpr int kChunk = 64 / TT;  // parts whose loads are in flight together
+    constexpr int kQ = TT / 4;       // float4 per row of a part and sweep
     cur.g = 0;
     cur.enter_group(part);
-    // Every CTA waits for the GEMV, also those with nothing to sum: this grid
-    // must not complete before the GEMV does, since the next kernel on the
-    // stream (possibly the next call, reading Y) waits only for this one.
-    griddep_wait();
-    if (np <= 1) return;  // finished whole by the GEMV
-    const int r = threadIdx.x, row = (int)cur.rb * kUnitRows + r;
     float acc[16];
 #pragma unroll
     for (int t = 0; t < 16; ++t) acc[t] = 0.f;
@@ -737,7 +778,7 @@ __global__ void __maxnreg__(kTcReduceRegs) tc_reduce_kernel(const StreamParams p
         for (int j = 0; j < kChunk; ++j) {
             if (j0 + j < np) {
                 const float4 *src = reinterpret_cast<const float4 *>(
-                    p.partials + (size_t)cur.next(part) * kTcPartialFloats + (size_t)r * T);
+                    p.partials + (size_t)cur.next(part) * tc_partial_floats(T) + (size_t)r * T + h * TT);
 #pragma unroll
                 for (int q = 0; q < kQ; ++q) f[j][q] = __ldcg(src + q);
             }
@@ -756,13 +797,77 @@ __global__ void __maxnreg__(kTcReduceRegs) tc_reduce_kernel(const StreamParams p
             }
         }
     }
-    tc_store_row(p, acc, row, __ldg(p.gscale) * kTcXUnscale);
+    tc_store_row(p, acc, row, __ldg(p.gscale) * kTcXUnscale, h * TT);
+}
+
+template <int T>
+__global__ void __maxnreg__(kTcReduceRegs) tc_reduce_kernel(const StreamParams p, const TcPartition part) {
+    griddep_launch_dependents();
+    constexpr int TT = T < 16 ? T : 16;  // tokens summed per sweep over the parts (T = 32: two sweeps)
+    TcPartCursor cur;
+    cur.rb = blockIdx.x;
+    cur.G = part.groups;
+    cur.KC = p.KC;
+    int np = 0;
+    for (cur.g = 0; (int)cur.g < cur.G; ++cur.g) {
+        cur.enter_group(part);
+        np += (int)cur.parts_in_group();
+    }
+    // Every CTA waits for the GEMV, also those with nothing to sum: this grid
+    // must not complete before the GEMV does, since the next kernel on the
+    // stream (possibly the next call, reading Y) waits only for this one.
+    griddep_wait();
+    if (np <= 1) return;  // finished whole by the GEMV
+    const int r = threadIdx.x, row = (int)cur.rb * kUnitRows + r;
+    if constexpr (T == 32) {
+        tc_reduce_sweep<T, TT>(p, part, cur, np, r, row, 0);
+        tc_reduce_sweep<T, TT>(p, part, cur, np, r, row, 1);
+    } else {
+        tc_reduce_sweep<T, TT>(p, part, cur, np, r, row, 0);
+    }
+}
+
+// X of one pass as f16 x 2^-8 for the 32-token kernel (which stages no bf16):
+// 8 elements (16 bytes) per thread and step; |x| >= 2^24 sets error bit 8.
+__global__ void __launch_bounds__(256) tc_x16_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ x16,
+                                                     long long chunks, unsigned *err) {
+    griddep_wait();  // X may be the output of the kernel ahead of this one
+    griddep_launch_dependents();
+    uint32_t bad = 0;
+    for (long long c = (long long)blockIdx.x * 256 + threadIdx.x; c < chunks; c += (long long)gridDim.x * 256) {
+        uint4 v = __ldg(reinterpret_cast<const uint4 *>(x) + c);
+        v.x = bf16x2_to_f16x2_scaled(v.x, bad);
+        v.y = bf16x2_to_f16x2_scaled(v.y, bad);
+        v.z = bf16x2_to_f16x2_scaled(v.z, bad);
+        v.w = bf16x2_to_f16x2_scaled(v.w, bad);
+        reinterpret_cast<uint4 *>(x16)[c] = v;
+    }
+    if (bad) atomicOr(err, kDevErrXRange);
+}
+
+cudaError_t launch_tc_x16(const uint16_t *x, uint16_t *x16, int n, int K, unsigned *err, cudaStream_t stream) {
+    const long long chunks = (long long)n * K / 8;
+    long long blocks = (chunks + 255) / 256;
+    if (blocks > 1024) blocks = 1024;
+    if (blocks < 1) blocks = 1;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_x16_kernel, x, x16, chunks, err);
 }
 
 cudaError_t tc_set_smem_limit(int smem_optin) {
     cudaError_t e = cudaFuncSetAttribute(gemv_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(gemv_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+    e = cudaFuncSetAttribute(gemv_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gemv_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
 }
 
 cudaError_t launch_tc(const CUtensorMap &tw, const CUtensorMap &ts, const CUtensorMap &tx, const StreamParams &p,
@@ -777,8 +882,9 @@ cudaError_t launch_tc(const CUtensorMap &tw, const CUtensorMap &ts, const CUtens
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = T == 16 ? cudaLaunchKernelEx(&cfg, gemv_tc_kernel<16>, tw, ts, tx, p, part)
-                            : cudaLaunchKernelEx(&cfg, gemv_tc_kernel<8>, tw, ts, tx, p, part);
+    cudaError_t e = T == 32   ? cudaLaunchKernelEx(&cfg, gemv_tc_kernel<32>, tw, ts, tx, p, part)
+                    : T == 16 ? cudaLaunchKernelEx(&cfg, gemv_tc_kernel<16>, tw, ts, tx, p, part)
+                              : cudaLaunchKernelEx(&cfg, gemv_tc_kernel<8>, tw, ts, tx, p, part);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t rc = {};
     rc.gridDim = dim3(part.row_blocks);
@@ -786,8 +892,9 @@ cudaError_t launch_tc(const CUtensorMap &tw, const CUtensorMap &ts, const CUtens
     rc.stream = stream;
     rc.attrs = attr;
     rc.numAttrs = 1;
-    return T == 8 ? cudaLaunchKernelEx(&rc, tc_reduce_kernel<8>, p, part)
-                  : cudaLaunchKernelEx(&rc, tc_reduce_kernel<16>, p, part);
+    return T == 32   ? cudaLaunchKernelEx(&rc, tc_reduce_kernel<32>, p, part)
+           : T == 16 ? cudaLaunchKernelEx(&rc, tc_reduce_kernel<16>, p, part)
+                     : cudaLaunchKernelEx(&rc, tc_reduce_kernel<8>, p, part);
 }
 
 }  // namespace nvfp4

@@ -20,6 +20,7 @@ constexpr int kSTileBytes = kUnitRows * 16;             // 2048 (16 scale bytes 
 constexpr int kStageBytes = kWTileBytes + kSTileBytes;  // 10240
 constexpr int kMaxStages = 8;
 constexpr int kMaxTokensPerPass = 16;
+constexpr int kTcMaxTokensPerPass = 32;  // tcgen05 kernel with the X ring
 constexpr int kSlotFloats = 32 * 16;  // one warp's partial tile: 32 lanes x 16 fp32
 constexpr int kCountersPerCta = 8;    // split-tile counters per CTA (one per fixup warp)
 
@@ -108,6 +109,12 @@ cudaError_t device_error_word(unsigned **ptr);  // device address of the error w
 constexpr int kTcUnitKHost = 256;
 constexpr int kTcMaxGroups = 32;
 constexpr int kTcMaxParts = 256;   // most parts of one split row block
+// fp32 partial tile of one (CTA, row-block segment) of the tcgen05 kernel:
+// 128 rows x max(T, 16) tokens
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+constexpr int tc_partial_floats(int T) { return kUnitRows * (T < 16 ? 16 : T); }
 constexpr int kTcReduceChunk = 4;  // partial tiles whose loads the reduction keeps in flight at once
 struct TcPartition {
     int groups;
@@ -127,8 +134,14 @@ cudaError_t tc_set_smem_limit(int smem_optin);
 // zeros).  With T = 8 the kernel bulk-copies X rows from p.x itself.
 // Launches the GEMV and then the split-row reduction, both with programmatic
 // dependent launch.
+// T = 32: tx views the pass's f16 X (written by launch_tc_x16) with box
+// {64, 32, 4}.
 cudaError_t launch_tc(const CUtensorMap &tw, const CUtensorMap &ts, const CUtensorMap &tx, const StreamParams &p,
                       const TcPartition &part, int T, int smem, cudaStream_t stream);
+// x16[t][k] = f16(x[t][k] * 2^-8) for the 32-token kernel (programmatic
+// dependent launch; |x| >= 2^24 sets device error bit 8).  x, x16 16-byte
+// aligned, n * K a multiple of 8.
+cudaError_t launch_tc_x16(const uint16_t *x, uint16_t *x16, int n, int K, unsigned *err, cudaStream_t stream);
 
 // Workspace a call needs (host-side plan; no GPU work): bytes of the zeroed
 // counter region at offset 0 and in total.  Returns an nvfp4_status.

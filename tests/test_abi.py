@@ -118,8 +118,15 @@ def test_one_pass_plan():
         mma = nv.nvfp4_gemv_plan(n, 14336, 5120, variant=nv.VARIANT_MMA)
         assert mma["units"] == (14336 // 128) * (5120 // 128)
         assert 2 <= plan["stages"] <= 8 and plan["stages"] % 2 == 0 and plan["smem_bytes"] <= 232448
-    # more than 16 tokens: chunks of 16
-    assert nv.nvfp4_gemv_plan(20, 4096, 4096)["tile_tokens"] == [16, 4]
+    # more than 16 tokens: one pass of up to 32 (X streamed per unit), then more
+    assert nv.nvfp4_gemv_plan(20, 4096, 4096)["tile_tokens"] == [20]
+    assert nv.nvfp4_gemv_plan(32, 14336, 5120)["tile_tokens"] == [32]
+    assert nv.nvfp4_gemv_plan(64, 14336, 5120)["tile_tokens"] == [32, 32]
+    assert nv.nvfp4_gemv_plan(40, 14336, 5120)["tile_tokens"] == [32, 8]
+    # a declared scratch size too small for the 32-token pass: 16-token passes
+    small = nv.nvfp4_gemv_workspace_size(16, 14336, 5120)
+    assert nv.nvfp4_gemv_workspace_size(32, 14336, 5120) > small
+    assert nv.nvfp4_gemv_plan(40, 14336, 5120, workspace_bytes=small)["tile_tokens"] == [16, 16, 8]
     # K too large for 16 tokens of X in shared memory: smaller chunks
     p = nv.nvfp4_gemv_plan(16, 1024, 8192)
     assert p["tile_tokens"] == [16]        # tcgen05: X is streamed per unit, any K fits

@@ -1,0 +1,151 @@
+"""GPU parity of the mid-M path (n = 17..64 tokens): the tcgen05 kernel with 32
+staged tokens, X converted once to f16 x 2^-8 and streamed per unit through a
+ring, up to 32 tokens per read of W (atlas #266 tile GEMM for the verify and
+prefill widths).
+
+Tolerance as for the GEMV: |y_gpu - y_ref| <= 1e-2 * (|y_ref| + 1), y_ref the
+oracle's unrounded fp64 value.  The k-group partition is the one of n <= 16,
+so a batched call still equals the single-token calls bit for bit (atlas #266,
+"Correctness argument").  Inputs: oracle-quantized W ~ N(0, 0.02), X ~ N(0, 1)
+bf16 (synth.py).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_weight_quantized_gemv_gb300 as nv
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    nv.build()
+    oracle.build()
+
+
+def make_case(N, K, n, wseed=0, xseed=1, outlier=0.0):
+    w = synth.weights_f32(N, K, wseed)
+    packed, scale, g = oracle.quantize(w)
+    x = synth.activations_bf16(n, K, xseed, outlier)
+    return packed, scale, g, x
+
+
+def to_gpu(packed, scale, g, x):
+    wp = torch.from_numpy(np.ascontiguousarray(packed)).cuda()
+    ws = torch.from_numpy(np.ascontiguousarray(scale)).cuda()
+    gs = torch.tensor([g], dtype=torch.float32, device="cuda")
+    xt = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda().view(torch.bfloat16)
+    return wp, ws, gs, xt
+
+
+def bits(t):
+    torch.cuda.synchronize()
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def as_f64(y16):
+    return torch.from_numpy(np.ascontiguousarray(y16).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def assert_close(y16, y64):
+    err = np.abs(as_f64(y16) - y64)
+    bad = ~(err <= TOL * (np.abs(y64) + 1.0))
+    assert not bad.any(), f"{bad.sum()} of {bad.size} out of tolerance; worst {err.max()}"
+
+
+@pytest.mark.parametrize("N,K,n,tiles", [
+    (1000, 1024, 17, [17]),        # one 32-token pass, 15 zero-filled token rows
+    (384, 2048, 32, [32]),         # a full pass
+    (2000, 512, 24, [24]),         # short segments (two units per row block)
+    (256, 8192, 20, [20]),         # deep K: several k-groups, many split parts
+    (700, 1280, 40, [32, 8]),      # a second pass of 8 tokens with the 32-token kernel
+    (300, 768, 64, [32, 32]),      # ragged rows, two full passes
+    (129, 256, 33, [32, 1]),       # one unit per row block, a one-token tail pass
+])
+def test_mid_m_full_output(N, K, n, tiles):
+    assert nv.nvfp4_gemv_plan(n, N, K)["tile_tokens"] == tiles
+    packed, scale, g, x = make_case(N, K, n, 3, 4, outlier=0.01)
+    y64, _ = oracle.gemv(packed, scale, g, x)
+    wp, ws, gs, xt = to_gpu(packed, scale, g, x)
+    assert_close(bits(nv.nvfp4_gemv_batched(wp, ws, gs, xt)), y64)
+
+
+@pytest.mark.parametrize("n", [32, 40])
+def test_mid_m_equals_single_token_calls(n):
+    N, K = 1536, 2048
+    packed, scale, g, x = make_case(N, K, n, 5, 6)
+    wp, ws, gs, xt = to_gpu(packed, scale, g, x)
+    full = bits(nv.nvfp4_gemv_batched(wp, ws, gs, xt))
+    for t in range(n):
+        one = bits(nv.nvfp4_gemv_batched(wp, ws, gs, xt[t:t + 1].contiguous()))
+        assert np.array_equal(one[0], full[t]), t
+
+
+@pytest.mark.parametrize("n", [32, 64])
+def test_mid_m_full_size_qkv_sampled(n):
+    N, K = 14336, 5120
+    packed, scale, g, x = make_case(N, K, n, 0, 1)
+    wp, ws, gs, xt = to_gpu(packed, scale, g, x)
+    y16 = bits(nv.nvfp4_gemv_batched(wp, ws, gs, xt))
+    assert not np.isnan(as_f64(y16)).any()
+    rng = np.random.Generator(np.random.PCG64(40 + n))
+    rows = np.concatenate([[0, 1, 127, 128, N - 129, N - 128, N - 1], rng.integers(0, N, 400)])
+    toks = rng.integers(0, n, rows.shape[0])
+    ref64, _ = oracle.gemv_points(packed, scale, g, x, toks, rows)
+    assert_close(y16[toks, rows], ref64)
+    for t in (0, 17, n - 1):  # batched == single token on the full-size launch configuration
+        one = bits(nv.nvfp4_gemv_batched(wp, ws, gs, xt[t:t + 1].contiguous()))
+        assert np.array_equal(one[0], y16[t]), t
+
+
+def test_mid_m_activation_beyond_f16_range_is_rescaled():
+    N, K, n = 256, 1024, 20
+    packed, scale, g, _ = make_case(N, K, 1, 1, 1)
+    xf = synth.activations_f32(n, K, 1)
+    xf[1, 17] = 3.0e5             # beyond f16's range, inside the 2^-8 prescale's
+    xf[19, 900] = -1.0e6
+    x = synth.to_bf16_bits(xf)
+    y64, _ = oracle.gemv(packed, scale, g, x)
+    wp, ws, gs, xt = to_gpu(packed, scale, g, x)
+    assert_close(bits(nv.nvfp4_gemv_batched(wp, ws, gs, xt)), y64)
+    assert nv.nvfp4_device_error() == 0
+
+
+def test_mid_m_swiglu():
+    F, K, n = 1024, 2048, 24
+    w = np.empty((2 * F, K), dtype=np.float32)
+    w[0::2] = synth.weights_f32(F, K, 7)
+    w[1::2] = synth.weights_f32(F, K, 8)
+    packed, scale, g = oracle.quantize(w)
+    x = synth.activations_bf16(n, K, 9)
+    h64, _ = oracle.gemv_swiglu(packed, scale, g, x)
+    wp, ws, gs, xt = to_gpu(packed, scale, g, x)
+    assert_close(bits(nv.nvfp4_gemv_swiglu(wp, ws, gs, xt)), h64)
+
+
+def test_mid_m_caller_workspace_and_fallback():
+    N, K, n = 2048, 2048, 32
+    packed, scale, g, x = make_case(N, K, n, 2, 3)
+    y64, _ = oracle.gemv(packed, scale, g, x)
+    wp, ws, gs, xt = to_gpu(packed, scale, g, x)
+    big = torch.zeros(nv.nvfp4_gemv_workspace_size(n, N, K), dtype=torch.uint8, device="cuda")
+    y_big = bits(nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt, workspace=big))
+    assert_close(y_big, y64)
+    # a scratch sized for 16 tokens: the call takes 16-token passes instead, same bits
+    small_bytes = nv.nvfp4_gemv_workspace_size(16, N, K)
+    assert small_bytes < big.numel()
+    small = torch.zeros(small_bytes, dtype=torch.uint8, device="cuda")
+    assert np.array_equal(bits(nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt, workspace=small)), y_big)
+    y = torch.empty((n, N), dtype=torch.bfloat16, device="cuda")
+    nv.nvfp4_gemv_batched_noalloc(wp, ws, gs, xt, y)
+    assert np.array_equal(bits(y), y_big)
+
+
+def test_no_device_error_recorded():
+    assert nv.nvfp4_device_error() == 0
