@@ -2,7 +2,7 @@
 """Benchmark of the NVFP4 batched decode GEMV on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload attn_qkv|o_proj|fused_qkv|decode_step] [--tiling one_pass|greedy_321]
+                    [--workload attn_qkv|o_proj|fused_qkv|mid_m|decode_step|ffn_verify|moe_decode] [--tiling one_pass|greedy_321]
 
 Prints ONE JSON line (rank 0).  A step is one pass of the hot path over one
 batch: for the default workload (attention qkv projection, N=14336, K=5120)
@@ -61,6 +61,8 @@ def workload_calls(name: str, n_sweep: int):
         return [("o_proj", 8)]
     if name == "fused_qkv":
         return [("fused_qkv", 16)]
+    if name == "mid_m":  # verify / prefill widths: one call of n tokens (n = 17..64)
+        return [("attn_qkv", n_sweep)]
     if name == "decode_step":
         return [(s, n_sweep) for _ in range(16) for s in ("attn_qkv", "o_proj")]
     if name == "ffn_verify":
@@ -402,9 +404,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="attn_qkv",
-                    choices=["attn_qkv", "o_proj", "fused_qkv", "decode_step", "ffn_verify", "moe_decode"])
+                    choices=["attn_qkv", "o_proj", "fused_qkv", "mid_m", "decode_step", "ffn_verify", "moe_decode"])
     ap.add_argument("--n", type=int, default=8,
-                    help="tokens per call for --workload decode_step / ffn_verify / moe_decode")
+                    help="tokens per call for --workload mid_m / decode_step / ffn_verify / moe_decode")
     ap.add_argument("--tiling", default="one_pass", choices=["one_pass", "greedy_321"])
     ap.add_argument("--variant", default="auto", choices=["auto", "mma", "simt", "generic"])
     ap.add_argument("--cpu-rows", type=int, default=96, help="oracle sample rows per host core and call")
@@ -423,6 +425,7 @@ def main():
         "attn_qkv": "attention qkv projection N=14336 K=5120, n=1,2,3,4 (one call each per step)",
         "o_proj": "output projection N=5120 K=6144, n=8, activations with 1% x20 outliers",
         "fused_qkv": "fused projection N=16384 K=5120, n=16",
+        "mid_m": f"attention qkv projection N=14336 K=5120, n={args.n} (mid-M: one read of W per 32 tokens)",
         "decode_step": f"decode step: 16 x (qkv N=14336 K=5120, o_proj N=5120 K=6144), n={args.n}",
         "ffn_verify": f"dense SwiGLU verify FFN D=5120 F=17408 (gate/up GEMV with fused SwiGLU, then down), "
                       f"n={args.n}",
