@@ -217,13 +217,16 @@ nvfp4_status nvfp4_ffn_swiglu(const uint8_t *w_gu_packed, const uint8_t *w_gu_sc
  * w_global_scale_f32 [E]: device; x_bf16 [n_tokens][K]: device, 16-byte
  * aligned; expert_offsets [E+1] and sorted_token [A] (int32): device;
  * y_bf16 [A][N] (swiglu: [A][N/2]): device, written, row j = assignment j.
- * E >= 1, A >= 0 (0: no-op), n_tokens >= 1, N a positive multiple of 16,
- * K a multiple of 32 in [32, 7168] whose 16 staged tokens (8 with swiglu) and
- * 16 weight rows fit shared memory (K <= 5632 without swiglu).  Each CTA
- * bulk-copies one contiguous block of an expert's rows, so each routed
- * expert is read once whatever its token count.  Asynchronous on `stream`;
- * one launch.  Errors: NVFP4_ERR_INVALID_ARG, NVFP4_ERR_MISALIGNED,
- * NVFP4_ERR_UNSUPPORTED (K too large), NVFP4_ERR_CUDA.
+ * 1 <= E <= 1024, A >= 0 (0: no-op), n_tokens >= 1, N a positive multiple
+ * of 16, K a multiple of 32 in [32, 7168].  K % 256 == 0: a persistent grid
+ * (one CTA per SM) streams the row blocks of the experts that have tokens
+ * through a ring of shared-memory slots (TMA) and multiplies on tensor cores
+ * (mma.sync, f16 x f16 -> fp32); other K: one CTA per (expert, row block),
+ * bulk-copied, SIMT FMAs (whose 16 staged tokens, 8 with swiglu, and 16
+ * weight rows must fit shared memory: K <= 5632 without swiglu).  Either
+ * way each routed expert is read once whatever its token count.
+ * Asynchronous on `stream`; one launch.  Errors: NVFP4_ERR_INVALID_ARG,
+ * NVFP4_ERR_MISALIGNED, NVFP4_ERR_UNSUPPORTED (K too large), NVFP4_ERR_CUDA.
  * Offsets outside [0, A] or decreasing and token indices outside
  * [0, n_tokens) are skipped by the kernel and set bit 32 of the device error
  * word (nvfp4_device_error).

@@ -81,6 +81,8 @@ static nvfp4_status device_state(int dev, DeviceState **out) {
             return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory, tcgen05 kernel)");
         if ((e = moe_set_smem_limit(d.smem_optin)) != cudaSuccess)
             return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory, grouped expert kernel)");
+        if ((e = moe_mma_set_smem_limit(d.smem_optin)) != cudaSuccess)
+            return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory, tensor-core expert kernel)");
         if ((e = device_error_word(&d.err_word)) != cudaSuccess)
             return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
         d.ready = true;
@@ -638,8 +640,9 @@ extern "C" nvfp4_status nvfp4_moe_gemv_grouped(const uint8_t *w_packed, const ui
                                                int swiglu, cudaStream_t stream) {
     if (!w_packed || !w_scale_e4m3 || !w_global_scale_f32 || !x_bf16 || !expert_offsets || !sorted_token || !y_bf16)
         return fail(NVFP4_ERR_INVALID_ARG, "null pointer argument");
-    if (E < 1 || A < 0 || n_tokens < 1 || N < 1)
-        return fail(NVFP4_ERR_INVALID_ARG, "E = %d, A = %d, n_tokens = %d, N = %d out of range", E, A, n_tokens, N);
+    if (E < 1 || E > kMoeMaxExperts || A < 0 || n_tokens < 1 || N < 1)
+        return fail(NVFP4_ERR_INVALID_ARG, "E = %d (1..%d), A = %d, n_tokens = %d, N = %d out of range", E,
+                    kMoeMaxExperts, A, n_tokens, N);
     if (swiglu != 0 && swiglu != 1) return fail(NVFP4_ERR_INVALID_ARG, "swiglu must be 0 or 1");
     if (N % 16 != 0) return fail(NVFP4_ERR_INVALID_ARG, "N = %d must be a multiple of 16", N);
     if (K < 32 || K % 32 != 0 || K > kMoeMaxK)
@@ -671,7 +674,19 @@ extern "C" nvfp4_status nvfp4_moe_gemv_grouped(const uint8_t *w_packed, const ui
     p.N = N;
     p.K = K;
     p.swiglu = swiglu;
+    // K % 256 == 0: the streaming tensor-core kernel (W as 128-byte-swizzled TMA boxes)
+    if (moe_mma_plan(N, K, d->smem_optin, &p.item_rows, &p.stages, &p.tok_pass)) {
+        CUtensorMap tw;
+        if ((st = encode_2d(&tw, w_packed, (uint64_t)K / 2, (uint64_t)E * N, 128, (uint32_t)p.item_rows,
+                            CU_TENSOR_MAP_SWIZZLE_128B)) != NVFP4_OK)
+            return st;
+        p.ctas = d->sms;
+        p.rows_per_cta = p.row_groups = 0;
+        if ((e = launch_moe_mma(tw, p, stream)) != cudaSuccess) return cuda_fail(e, "grouped expert kernel launch");
+        return NVFP4_OK;
+    }
     const int out_rows = swiglu ? N / 2 : N;
+    p.item_rows = p.stages = p.tok_pass = p.ctas = 0;
     p.rows_per_cta = moe_rows_per_cta(K, swiglu != 0, d->smem_optin);
     if (p.rows_per_cta == 0)
         return fail(NVFP4_ERR_UNSUPPORTED, "K = %d: the staged tokens and 16 weight rows do not fit shared memory", K);

@@ -53,10 +53,22 @@ struct MoeParams {
     uint16_t *y;        // [A][N] (or [A][N/2] with swiglu)
     unsigned *err;      // device error word
     int E, A, ntok, N, K, swiglu;
-    int rows_per_cta;   // output rows (gate/up pairs with swiglu) per CTA
-    int row_groups;     // CTAs per expert
+    int rows_per_cta;   // SIMT kernel: output rows (gate/up pairs with swiglu) per CTA
+    int row_groups;     // SIMT kernel: CTAs per expert
+    int item_rows;      // tensor-core kernel: W rows per streamed item (128, 64, 32 or 16)
+    int stages;         // tensor-core kernel: items in flight per CTA (ring slots)
+    int tok_pass;       // tensor-core kernel: tokens staged per pass over an item (<= 16)
+    int ctas;           // tensor-core kernel: persistent grid (one CTA per SM)
 };
 constexpr int kMoeMaxK = 7168;
+constexpr int kMoeMaxExperts = 1024;
+constexpr int kMoeMaxStages = 8;
+constexpr int kMoeMmaStaticSmem = 5 * 1024;  // the tensor-core kernel's static shared memory, rounded up
+// Tensor-core kernel (moe_mma.cu, K % 256 == 0): plan, shared memory, launch.
+bool moe_mma_plan(int N, int K, int smem_optin, int *item_rows, int *stages, int *tok_pass);
+int moe_mma_smem_bytes(const MoeParams &p);
+cudaError_t moe_mma_set_smem_limit(int smem_optin);
+cudaError_t launch_moe_mma(const CUtensorMap &tw, const MoeParams &p, cudaStream_t stream);
 int moe_smem_bytes(int K, int rows_per_cta, bool swiglu);
 int moe_rows_per_cta(int K, bool swiglu, int smem_optin);  // 0: K too large for shared memory
 cudaError_t moe_set_smem_limit(int smem_optin);

@@ -74,6 +74,7 @@ def test_grouped_expert_validation_without_gpu():
     f = L.nvfp4_moe_gemv_grouped
     assert f(None, a, a, a, a, a, a, 4, 8, 2, 64, 256, 0, None) == nv.NVFP4_ERR_INVALID_ARG
     assert f(a, a, a, a, a, a, a, 0, 8, 2, 64, 256, 0, None) == nv.NVFP4_ERR_INVALID_ARG      # E
+    assert f(a, a, a, a, a, a, a, 1025, 8, 2, 64, 256, 0, None) == nv.NVFP4_ERR_INVALID_ARG   # E > 1024
     assert f(a, a, a, a, a, a, a, 4, 8, 2, 64, 240, 0, None) == nv.NVFP4_ERR_INVALID_ARG      # K % 32
     assert f(a, a, a, a, a, a, a, 4, 8, 2, 64, 8192, 0, None) == nv.NVFP4_ERR_INVALID_ARG     # K too large
     assert f(a, a, a, a, a, a, a, 4, 8, 2, 72, 256, 1, None) == nv.NVFP4_ERR_INVALID_ARG      # N % 16

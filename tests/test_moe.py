@@ -84,9 +84,14 @@ def run(packed, scale, g, x, off, tok, swiglu=False):
     return host_bits(y)
 
 
-@pytest.mark.parametrize("E,N,K,n,topk,swiglu", [(8, 256, 512, 4, 2, False), (16, 320, 1024, 16, 4, False),
-                                                 (8, 256, 2048, 12, 3, True), (4, 96, 4096, 3, 2, False),
-                                                 (3, 48, 5632, 18, 2, False)])
+@pytest.mark.parametrize("E,N,K,n,topk,swiglu", [
+    # K % 256 == 0: the streaming tensor-core kernel
+    (8, 256, 512, 4, 2, False), (16, 320, 1024, 16, 4, False), (8, 256, 2048, 12, 3, True),
+    (4, 96, 4096, 3, 2, False), (3, 48, 5632, 18, 2, False),
+    (24, 1536, 2048, 16, 8, True), (24, 2048, 768, 16, 8, False),   # the bench's expert shapes
+    (5, 16, 7168, 20, 2, True),                                      # deepest K: fewer staged tokens per pass
+    # other K: the SIMT kernel
+    (6, 128, 800, 7, 2, False), (4, 64, 352, 5, 3, True)])
 def test_grouped_matches_oracle(E, N, K, n, topk, swiglu):
     packed, scale, g = experts(E, N, K, seed=N + K, swiglu=swiglu)
     x = synth.activations_bf16(n, K, seed=5)
