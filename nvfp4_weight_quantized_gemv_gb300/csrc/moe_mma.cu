@@ -83,11 +83,9 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t sc2, uint32_t 
     a[3] = hmul2_u32(e2m1x2_to_f16x2<3>(w), sc2);
 }
 
-// E4M3 byte `i` (0..15) of a 16-byte scale vector -> f16 in both halves.
-__device__ __forceinline__ uint32_t scale_dup(const uint4 &s4, int i) {
-    const uint32_t word = (i < 8) ? ((i < 4) ? s4.x : s4.y) : ((i < 12) ? s4.z : s4.w);
-    const uint32_t b = (word >> (8 * (i & 3))) & 0xFFu;
-    return dup_lo(e4m3x2_to_f16x2(b));
+// Bytes 0 and 2 of `w` (two E4M3 scales) -> f16x2 {byte 0, byte 2}.
+__device__ __forceinline__ uint32_t scales02_to_f16x2(uint32_t w) {
+    return e4m3x2_to_f16x2(__byte_perm(w, 0u, 0x0020));
 }
 
 template <bool SWIGLU>
@@ -178,8 +176,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // ------------------------------------------------------------ consumers
     const int ngroups = IR >> 4, kparts = kMmaWarps / ngroups;
     const int gi = warp % ngroups, kp = warp / ngroups;
-    const int nch = KC * 8;  // 32-k chunks
-    const int ch0 = kp * nch / kparts, ch1 = (kp + 1) * nch / kparts;
+    const int b0 = kp * KC / kparts, b1 = (kp + 1) * KC / kparts;  // this warp's 256-k boxes
     const int g = lane >> 2, q = lane & 3;
     const int r0 = gi * 16 + g;  // this lane's rows r0 and r0 + 8 of the item
     uint32_t bad = 0;
@@ -230,25 +227,39 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 const uint32_t xr0 = xs + (uint32_t)n0 * x_pitch + (uint32_t)q * 16;
                 const uint32_t xr1 = xs + (uint32_t)n1 * x_pitch + (uint32_t)q * 16;
                 const uint32_t sw = (uint32_t)(r0 & 7);  // 128-byte swizzle phase of rows r0 and r0 + 8
-                uint4 sa = make_uint4(0, 0, 0, 0), sb = sa;
-                for (int ch = ch0; ch < ch1; ++ch) {
-                    const int b = ch >> 3, cb = ch & 7;
-                    if (cb == 0 || ch == ch0) {  // the 16 scales of box b for rows r0 and r0 + 8
-                        sa = lds128(ssm + (uint32_t)r0 * srow + b * 16);
-                        sb = lds128(ssm + (uint32_t)(r0 + 8) * srow + b * 16);
-                    }
-                    const uint32_t woff = wsm + (uint32_t)b * box_bytes + (((uint32_t)cb ^ sw) << 4) + q * 4;
-                    const uint32_t wa = lds32(woff + (uint32_t)r0 * 128), wb = lds32(woff + (uint32_t)(r0 + 8) * 128);
-                    uint32_t aa[4], ab[4];
-                    dequant_word(wa, scale_dup(sa, 2 * cb + (q >> 1)), aa);  // k 8q..8q+7 of the chunk: one block
-                    dequant_word(wb, scale_dup(sb, 2 * cb + (q >> 1)), ab);
-                    const uint4 x0 = lds128(xr0 + (uint32_t)ch * 64);
-                    mma_16816(d[0], aa[0], ab[0], aa[1], ab[1], x0.x, x0.y);
-                    mma_16816(d[0], aa[2], ab[2], aa[3], ab[3], x0.z, x0.w);
-                    if (ntg > 1) {
-                        const uint4 x1 = lds128(xr1 + (uint32_t)ch * 64);
-                        mma_16816(d[1], aa[0], ab[0], aa[1], ab[1], x1.x, x1.y);
-                        mma_16816(d[1], aa[2], ab[2], aa[3], ab[3], x1.z, x1.w);
+                const int hq = q >> 1;                   // lane quad q covers 16-k block 2 cb + hq of chunk cb
+                for (int b = b0; b < b1; ++b) {
+                    // the box's 16 scales of rows r0 and r0 + 8, shifted so that byte 2j + 16m of word m is block
+                    // 2 (2m + j) + hq, i.e. the scale of chunk cb = 2m + j
+                    uint4 sa = lds128(ssm + (uint32_t)r0 * srow + b * 16);
+                    uint4 sb = lds128(ssm + (uint32_t)(r0 + 8) * srow + b * 16);
+                    const uint32_t shv = 8u * (uint32_t)hq;
+                    sa.x >>= shv; sa.y >>= shv; sa.z >>= shv; sa.w >>= shv;
+                    sb.x >>= shv; sb.y >>= shv; sb.z >>= shv; sb.w >>= shv;
+                    const uint32_t wbox = wsm + (uint32_t)b * box_bytes + q * 4;
+                    const uint32_t xo0 = xr0 + (uint32_t)b * 512, xo1 = xr1 + (uint32_t)b * 512;
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const uint32_t s2a = scales02_to_f16x2(m == 0 ? sa.x : m == 1 ? sa.y : m == 2 ? sa.z : sa.w);
+                        const uint32_t s2b = scales02_to_f16x2(m == 0 ? sb.x : m == 1 ? sb.y : m == 2 ? sb.z : sb.w);
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const int cb = 2 * m + j;
+                            const uint32_t woff = wbox + (((uint32_t)cb ^ sw) << 4);
+                            const uint32_t wa = lds32(woff + (uint32_t)r0 * 128);
+                            const uint32_t wb = lds32(woff + (uint32_t)(r0 + 8) * 128);
+                            uint32_t aa[4], ab[4];
+                            dequant_word(wa, j ? dup_hi(s2a) : dup_lo(s2a), aa);  // k 8q..8q+7: one scale block
+                            dequant_word(wb, j ? dup_hi(s2b) : dup_lo(s2b), ab);
+                            const uint4 x0 = lds128(xo0 + cb * 64);
+                            mma_16816(d[0], aa[0], ab[0], aa[1], ab[1], x0.x, x0.y);
+                            mma_16816(d[0], aa[2], ab[2], aa[3], ab[3], x0.z, x0.w);
+                            if (ntg > 1) {
+                                const uint4 x1 = lds128(xo1 + cb * 64);
+                                mma_16816(d[1], aa[0], ab[0], aa[1], ab[1], x1.x, x1.y);
+                                mma_16816(d[1], aa[2], ab[2], aa[3], ab[3], x1.z, x1.w);
+                            }
+                        }
                     }
                 }
             }
