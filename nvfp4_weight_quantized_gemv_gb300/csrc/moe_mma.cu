@@ -318,29 +318,31 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 }  // namespace
 
 // Items of 128, 64, 32 or 16 W rows (16-row groups times k parts = 8 warps):
-// the largest with at least three ring slots beside 16 staged tokens, else
-// with two, else fewer staged tokens; false if nothing fits.
+// the largest that leaves two ring slots beside 16 (else 8) staged tokens --
+// fewer k parts mean fewer partial sums to exchange per item (measured on the
+// 1536 x 2048 gate/up experts: 64 rows, 2 slots, 8 tokens 77 us per layer;
+// 32 rows, 3-4 slots 90 us; 16 rows, 7 slots 122 us) -- else fewer staged
+// tokens (deep K); false if even that does not fit.
 bool moe_mma_plan(int N, int K, int smem_optin, int *item_rows, int *stages, int *tok_pass) {
     if (K % 256 != 0) return false;
     const int budget = smem_optin - kMoeMmaStaticSmem - 1024 - 2 * kMmaWarps * 2 * 512;
-    for (int min_st = 3; min_st >= 2; --min_st) {
-        for (int tok = 16; tok >= 1; tok /= 2) {
-            const int room = budget - tok * (K * 2 + 64);
-            for (int rows = 128; rows >= 16; rows /= 2) {
-                if (rows > N && rows > 16) continue;
-                const int slot = ((K / 256) * rows * 128 + rows * (K / 16) + 1023) & ~1023;
-                int st = room / slot;
-                if (st > kMoeMaxStages) st = kMoeMaxStages;
-                if (st >= min_st) {
-                    *item_rows = rows;
-                    *stages = st;
-                    *tok_pass = tok;
-                    return true;
-                }
-            }
-            if (min_st == 3) break;  // with three slots, only 16 staged tokens are tried
-        }
-    }
+    auto fits = [&](int rows, int tok) {
+        if (rows > N && rows > 16) return false;
+        const int slot = ((K / 256) * rows * 128 + rows * (K / 16) + 1023) & ~1023;
+        int st = (budget - tok * (K * 2 + 64)) / slot;
+        if (st > kMoeMaxStages) st = kMoeMaxStages;
+        if (st < 2) return false;
+        *item_rows = rows;
+        *stages = st;
+        *tok_pass = tok;
+        return true;
+    };
+    for (int rows = 128; rows >= 16; rows /= 2)
+        for (int tok = 16; tok >= 8; tok /= 2)
+            if (fits(rows, tok)) return true;
+    for (int tok = 4; tok >= 1; tok /= 2)
+        for (int rows = 128; rows >= 16; rows /= 2)
+            if (fits(rows, tok)) return true;
     return false;
 }
 
