@@ -91,6 +91,7 @@ def peaks():
 # variant -> (kernel source, committed ncu summary, kernel name)
 KERNELS = {
     "tc": ("gemv_tc.cu", "gemv_tc_attn_qkv.md", "gemv_tc_kernel"),
+    "moe": ("moe_mma.cu", "moe_mma_moe_decode.md", "moe_mma_kernel"),
     "mma": ("gemv_stream.cu", "gemv_stream_mma_attn_qkv.md", "gemv_stream_kernel<mma>"),
     "simt": ("gemv_stream.cu", "gemv_stream_simt_attn_qkv.md", "gemv_stream_kernel<simt>"),
     "generic": ("gemv_generic.cu", "gemv_generic_attn_qkv.md", "gemv_generic_kernel"),
@@ -115,7 +116,7 @@ def kernel_traffic(variant):
                 return None, None
     except OSError:
         return None, None
-    m_tr = re.search(r"dram_bytes_per_launch_n(\d+):\s*([0-9]+)", text)
+    m_tr = re.search(r"dram_bytes_per_(?:launch|step)_n(\d+):\s*([0-9]+)", text)
     if not m_tr:
         return None, None
     return int(m_tr.group(2)), int(m_tr.group(1))
@@ -368,6 +369,13 @@ def run_moe(args, torch, nv, rank, world, local_rank, wl_desc, cores):
     if not args.no_cpu_baseline and world == 1:
         gbs, wall, sample = cpu_oracle_sample(workload_calls("moe_decode", n), args.cpu_rows, cores)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+    # ncu DRAM bytes of one step (both launches) from the committed summary, for n = 16 only
+    moe_traffic, moe_traffic_note = None, "null: no ncu counters for this kernel source and n"
+    tr, tr_n = kernel_traffic("moe")
+    if tr is not None and tr_n == n:
+        moe_traffic = tr
+        moe_traffic_note = (f"ncu dram read+write bytes of one captured step (gate/up + down) at n={n}; "
+                            "steps differ in their active experts")
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak",
@@ -380,10 +388,10 @@ def run_moe(args, torch, nv, rank, world, local_rank, wl_desc, cores):
         "per_call": {f"moe_step_n{n}": {"us_per_call": round(ms_per_step * 1e3, 3), "GB_s": round(achieved, 1),
                                         "frac_of_measured_hbm": round(achieved / hbm_peak, 4)}},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "frac": round(achieved / hbm_peak, 4), "traffic": moe_traffic,
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-                     "kernel": "moe_gemv_kernel", "algorithmic_bytes_per_step": round(mean_bytes),
-                     "traffic_note": "null: no ncu counters recorded for this workload"},
+                     "kernel": "moe_mma_kernel (gate/up + down)", "algorithmic_bytes_per_step": round(mean_bytes),
+                     "traffic_note": moe_traffic_note},
         "cpu_baseline": cpu,
         "e2e": {"value": round(world * mean_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2,
@@ -710,7 +718,9 @@ def main():
     e2e_ms = max_over_ranks(torch, dist, e2e_ms, dev)
     e2e_value = whole_job_gbs(world, step_bytes, e2e_ms)
 
-    traffic, traffic_n = kernel_traffic(plan["variant"]) if not is_ffn else (None, None)
+    # the recorded counters are of the attention qkv shape (N=14336, K=5120): other shapes report none
+    qkv_only = args.workload == "attn_qkv"
+    traffic, traffic_n = kernel_traffic(plan["variant"]) if qkv_only else (None, None)
     achieved = step_bytes / (ms_per_step * 1e-3) / 1e9  # per GPU: algorithmic bytes per launch / launch time
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
@@ -719,8 +729,9 @@ def main():
                 "frac_of_8TBs": round(achieved / NOMINAL_HBM_GBS, 4),
                 "kernel": KERNELS[plan["variant"]][2],
                 "algorithmic_bytes_per_step": step_bytes,
-                "traffic_note": (f"ncu dram read+write bytes per launch at n={traffic_n}" if traffic else
-                                 "null: the recorded ncu counters cover the attention qkv shape only" if is_ffn
+                "traffic_note": (f"ncu dram read+write bytes per launch at n={traffic_n} (attention qkv shape)"
+                                 if traffic else
+                                 "null: the recorded ncu counters cover the attention qkv shape only" if not qkv_only
                                  else "null: no ncu counters for the current kernel source")}
 
     if dist is not None:

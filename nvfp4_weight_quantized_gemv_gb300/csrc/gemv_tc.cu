@@ -3,7 +3,8 @@
 // Computes Y[t, r] = g * sum_k X[t, k] * E2M1(W[r, k]) * E4M3(S[r, k/16]) for all
 // n <= 16 tokens from ONE pass over W (atlas pull request #266, "What it
 // does": each tile of decode tokens reads the projection weight once; here
-// the tile is all n tokens).
+// the tile is all n tokens), and up to 32 tokens per pass in a 32-token mode
+// (below) for the mid-M widths.
 //
 // Work split.  The weight matrix is cut into units of 128 rows x 256 k (128 B
 // of every packed row + 16 scale bytes per row).  K is cut into `groups`
@@ -25,7 +26,12 @@
 // swizzled layout; rows n..7 are zeroed beforehand.  With T = 16 the X warp
 // loads one 3D TMA box per unit straight into the swizzled layout (rows
 // past n zero-filled) and the epilogue warps convert it in place.  No
-// separate conversion kernel or X buffer in global memory.
+// separate conversion kernel or X buffer in global memory.  With T = 32 the
+// group's X for 32 tokens would not fit beside the weight ring: X is
+// converted once per pass by tc_x16_kernel into the workspace and the X warp
+// streams each unit's {64 k, 32 tokens, 4} box into a ring of kTcXRing slots,
+// which the unit's two issuers release with a commit; same partition, so the
+// results equal those of n <= 16 calls bit for bit.
 //
 // Warp roles (576 threads, one CTA per SM):
 //   warp 0       weight producer: 2D TMA loads of the unit's W tile
