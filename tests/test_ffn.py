@@ -78,8 +78,9 @@ def test_gemv_swiglu_batched_equals_single_token_calls():
         assert np.array_equal(ht[0], hb[t]), t
 
 
-def test_ffn_swiglu_matches_oracle():
-    D, F, n = 1024, 2048, 4
+@pytest.mark.parametrize("n", [4, 24])  # 24: both projections take the 32-token mode
+def test_ffn_swiglu_matches_oracle(n):
+    D, F = 1024, 2048
     gu = joint_gate_up(F, D, seed=21)
     down = oracle.quantize(synth.weights_f32(D, F, 23))
     x = synth.activations_bf16(n, D, seed=24)
