@@ -147,5 +147,15 @@ def test_mid_m_caller_workspace_and_fallback():
     assert np.array_equal(bits(y), y_big)
 
 
+@pytest.mark.parametrize("num_ctas,stages", [(1, 2), (7, 4), (150, 8), (0, 2)])
+def test_mid_m_grid_and_ring_options(num_ctas, stages):
+    N, K, n = 700, 1280, 24
+    packed, scale, g, x = make_case(N, K, n, 7, 8)
+    y64, _ = oracle.gemv(packed, scale, g, x)
+    wp, ws, gs, xt = to_gpu(packed, scale, g, x)
+    y = nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt, variant=nv.VARIANT_TC, num_ctas=num_ctas, stages=stages)
+    assert_close(bits(y), y64)
+
+
 def test_no_device_error_recorded():
     assert nv.nvfp4_device_error() == 0
