@@ -46,11 +46,11 @@
 //                8 x tcgen05.mma.kind::f16 per half unit, M = 128 weight
 //                rows, N = 16 token columns, K = 16; A from tensor memory,
 //                B (= X) from shared memory.
-//   warps 6-13   dequantise: thread = weight row; warp (lane quarter q, k
-//                half j) turns rows 32q..32q+31, k 128j..128j+127 of every
-//                unit into f16 (E2M1 cvt times the E4M3 block scale: exact)
-//                and stores them with two tcgen05.st of 32 columns; the four
-//                warps of a k half hand that half of the A buffer over.
+//   warps 6-13   dequantise: thread = weight row; warp set b (warps 6-9,
+//                10-13) converts the units of A buffer b, warp (lane quarter
+//                q) all 256 k of rows 32q..32q+31 into f16 (E2M1 cvt times
+//                the E4M3 block scale: exact) with four tcgen05.st of 32
+//                columns, handing each 128-k half over as it is stored.
 //   warps 14-17  X conversion (bf16 -> f16 x 2^-8 in shared memory, unit by
 //                unit in the order the CTA uses them), then the epilogue:
 //                per finished row-block segment, tcgen05.ld of the
@@ -98,12 +98,12 @@ constexpr int kTcWarpProducer = 0;
 constexpr int kTcWarpX = 1;
 constexpr int kTcWarpIssuer0 = kTcWarpX + 1;                    // issuers: warps 2 ..
 constexpr int kTcWarpDequant0 = kTcWarpIssuer0 + kTcIssuers;    // dequant: the next 16 warps
-// Eight dequant warps of 128 k each measured as fast as sixteen of 64 k at
-// n <= 4 and faster at n = 16, with fewer threads and registers to spare.
+// Eight dequant warps in two sets of four: set b converts the units of A
+// buffer b, a warp all 256 k of its 32 rows, so each warp has two units'
+// time per unit it converts (its per-unit latencies -- barrier round trips,
+// shared-memory loads, the tensor-memory store -- overlap with the other
+// set's unit).
 constexpr int kTcDequantWarps = 8;
-constexpr int kTcDequantK = kTcUnitK * 4 / kTcDequantWarps;  // k of a unit per dequant warp (4 lane quarters)
-constexpr int kTcDqChunks = kTcDequantK / 32;                // 16-byte chunks of packed codes per lane
-constexpr int kTcDqStores = kTcDequantK / 64;                // 32-column tensor-memory stores per unit
 constexpr int kTcWarpEpilogue0 = kTcWarpDequant0 + kTcDequantWarps;  // epilogue: warps 14..17
 constexpr int kTcEpilogueWarps = 4;
 constexpr int kTcThreads = (kTcWarpEpilogue0 + kTcEpilogueWarps) * 32;  // 576
@@ -329,7 +329,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(sFull + 8 * s, 1);
-            mbar_init(sEmpty + 8 * s, kTcDequantWarps);
+            mbar_init(sEmpty + 8 * s, kTcDequantWarps / kTcABufs);
         }
         fence_barrier_init();
         const int pre = count < kTcStagesBeforeX ? count : (kTcStagesBeforeX < S ? kTcStagesBeforeX : S);
@@ -339,7 +339,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
             mbar_init(sXFull + 8 * s, kRing ? kTcIssuersPerBuf : kTcXConverterWarps);
         }
         for (int b = 0; b < kTcABufs * kTcAParts; ++b) {
-            mbar_init(sAFull + 8 * b, kTcDequantWarps / kTcAParts);
+            mbar_init(sAFull + 8 * b, kTcDequantWarps / kTcABufs);
             mbar_init(sAEmpty + 8 * b, 1);
         }
         for (int d = 0; d < 2 * kTcIssuers; ++d) mbar_init(sDFull + 8 * d, 1);
@@ -583,73 +583,73 @@ __global__ void __maxnreg__(kTcMaxRegs)
         __syncwarp();
     } else if (warp < kTcWarpEpilogue0) {
         // ------------------------------------------------------------ dequant
+        // Two sets of four warps: set ab converts the units of A buffer ab
+        // (i % 2 == ab), a warp (lane quarter lq) all 256 k of rows
+        // 32 lq .. 32 lq + 31; each warp has two units' time for one.
         const int e = warp - kTcWarpDequant0;  // 0 .. kTcDequantWarps - 1
         const int lq = warp & 3;               // tensor-memory lane quarter this warp may access
-        const int kw = e >> 2;                 // which kTcDequantK-wide k slice of the unit
-        const int part = kw * kTcDequantK / (kTcUnitK / kTcAParts);  // this warp's part of every A buffer
+        const int ab = e >> 2;                 // its A buffer: units i with i % kTcABufs == ab
         const int r = 32 * lq + lane;          // row within the unit
         const uint32_t lane_bits = (uint32_t)(32 * lq) << 16;
-        // this lane's kTcDequantK k of row r: kTcDqChunks swizzled 16-byte chunks
-        // of the packed row, and kTcDequantK / 16 scale bytes (4-byte aligned)
         const uint32_t w_row = (uint32_t)r * 128, w_sw = (uint32_t)(r & 7);
-        const uint8_t *const s_row = base + (sS - sW) + r * 16 + kw * (kTcDequantK / 16);
+        const uint8_t *const s_row = base + (sS - sW) + r * 16;
         bool ok = true;
-        int slot = 0, ab = 0;            // ring stage, A buffer (i % S, i % kTcABufs kept incrementally)
-        uint32_t fpar = 0, apar = 1;     // parities to wait for: full[slot]; aempty[ab] from round 1 on
-        for (int i = 0; i < count; ++i) {
+        int slot = ab % S;               // ring stage of unit i (advanced by kTcABufs per unit)
+        uint32_t fpar = 0, apar = 1;     // parities to wait for: full[slot]; aempty from round 1 on
+        for (int i = ab; i < count; i += kTcABufs) {
             if (__any_sync(0xffffffffu, !mbar_wait_bounded(sFull + 8 * slot, fpar))) {
                 ok = false;
                 break;
             }
             const uint32_t wst = sW + slot * kTcWBytes + w_row;
-            uint4 wv[kTcDqChunks];
+            uint4 wv[8];
 #pragma unroll
-            for (int j = 0; j < kTcDqChunks; ++j)
-                wv[j] = lds128(wst + ((((uint32_t)(kw * kTcDqChunks + j)) ^ w_sw) << 4));
-            uint32_t sv[kTcDqStores];
-#pragma unroll
-            for (int h = 0; h < kTcDqStores; ++h)
-                sv[h] = *reinterpret_cast<const uint32_t *>(s_row + slot * kTcSBytes + 4 * h);
+            for (int j = 0; j < 8; ++j) wv[j] = lds128(wst + ((((uint32_t)j) ^ w_sw) << 4));
+            const uint4 s16 = *reinterpret_cast<const uint4 *>(s_row + slot * kTcSBytes);
             __syncwarp();
             if (lane == 0) mbar_arrive(sEmpty + 8 * slot);  // the weight stage may be refilled
-            if (++slot == S) {
-                slot = 0;
+            slot += kTcABufs;
+            if (slot >= S) {  // S is even: every set sees every other stage, each phase
+                slot -= S;
                 fpar ^= 1u;
             }
-            if (i >= kTcABufs &&
-                __any_sync(0xffffffffu, !mbar_wait_bounded(sAEmpty + 8 * (ab * kTcAParts + part), apar))) {
-                ok = false;
-                break;
-            }
-            tc::fence_after_sync();  // the tensor-memory stores below follow the MMAs that read this part
+            const uint32_t svs[4] = {s16.x, s16.y, s16.z, s16.w};
 #pragma unroll
-            for (int h = 0; h < kTcDqStores; ++h) {  // 64 k (32 columns) per store
-                const uint32_t s01 = e4m3x2_to_f16x2(sv[h]), s23 = e4m3x2_to_f16x2(sv[h] >> 16);
-                const uint32_t sc[4] = {dup_lo(s01), dup_hi(s01), dup_lo(s23), dup_hi(s23)};
-                const uint32_t words[8] = {wv[2 * h].x, wv[2 * h].y, wv[2 * h].z, wv[2 * h].w,
-                                           wv[2 * h + 1].x, wv[2 * h + 1].y, wv[2 * h + 1].z, wv[2 * h + 1].w};
-                uint32_t v[32];
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    uint32_t f;
-                    switch (q & 3) {
-                        case 0: f = e2m1x2_to_f16x2<0>(words[q >> 2]); break;
-                        case 1: f = e2m1x2_to_f16x2<1>(words[q >> 2]); break;
-                        case 2: f = e2m1x2_to_f16x2<2>(words[q >> 2]); break;
-                        default: f = e2m1x2_to_f16x2<3>(words[q >> 2]); break;
-                    }
-                    v[q] = hmul2_u32(f, sc[q >> 3]);  // column q holds k pair (2q, 2q+1); 8 columns per scale block
+            for (int part = 0; part < kTcAParts; ++part) {
+                if (i >= kTcABufs &&
+                    __any_sync(0xffffffffu, !mbar_wait_bounded(sAEmpty + 8 * (ab * kTcAParts + part), apar))) {
+                    ok = false;
+                    break;
                 }
-                tc::st_32x32b_x32(tbase + lane_bits + ab * kTcAColsPerUnit + (kw * kTcDqStores + h) * 32, v);
+                tc::fence_after_sync();  // the tensor-memory stores below follow the MMAs that read this part
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {  // 64 k (32 columns) per store
+                    const int h = part * 2 + h2;
+                    const uint32_t s01 = e4m3x2_to_f16x2(svs[h]), s23 = e4m3x2_to_f16x2(svs[h] >> 16);
+                    const uint32_t sc[4] = {dup_lo(s01), dup_hi(s01), dup_lo(s23), dup_hi(s23)};
+                    const uint32_t words[8] = {wv[2 * h].x, wv[2 * h].y, wv[2 * h].z, wv[2 * h].w,
+                                               wv[2 * h + 1].x, wv[2 * h + 1].y, wv[2 * h + 1].z, wv[2 * h + 1].w};
+                    uint32_t v[32];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        uint32_t f;
+                        switch (q & 3) {
+                            case 0: f = e2m1x2_to_f16x2<0>(words[q >> 2]); break;
+                            case 1: f = e2m1x2_to_f16x2<1>(words[q >> 2]); break;
+                            case 2: f = e2m1x2_to_f16x2<2>(words[q >> 2]); break;
+                            default: f = e2m1x2_to_f16x2<3>(words[q >> 2]); break;
+                        }
+                        v[q] = hmul2_u32(f, sc[q >> 3]);  // column q holds k pair (2q, 2q+1); 8 columns per scale block
+                    }
+                    tc::st_32x32b_x32(tbase + lane_bits + ab * kTcAColsPerUnit + h * 32, v);
+                }
+                tc::wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sAFull + 8 * (ab * kTcAParts + part));
             }
-            tc::wait_st();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sAFull + 8 * (ab * kTcAParts + part));
-            if (++ab == kTcABufs) {  // next round R = i / kTcABufs + 1 waits for the phase of round R - 1
-                ab = 0;
-                apar ^= 1u;
-            }
+            if (!ok) break;
+            apar ^= 1u;  // the next unit of this buffer waits for the phase of this one
         }
         if (!ok && lane == 0) atomicOr(p.err, kDevErrTimeoutFull);
     } else {
