@@ -101,10 +101,14 @@ typedef struct nvfp4_gemv_plan_info {
  *
  * w_packed, w_scale_e4m3, w_global_scale_f32, x_bf16: device, read only.
  * y_bf16: device, written.  n >= 0 (n == 0 is a no-op), N >= 1, K >= 16 and
- * K % 16 == 0.  Any n is accepted; more than 16 tokens (or fewer when
- * n * K is too large for shared memory) are processed in chunks that each
- * re-read W.  The fast (tcgen05) path needs K % 256 == 0 and 16-byte aligned
- * w_packed, w_scale_e4m3 and x_bf16; other inputs take the GENERIC kernel.
+ * K % 16 == 0.  Any n is accepted.  The fast (tcgen05) path needs
+ * K % 256 == 0 and 16-byte aligned w_packed, w_scale_e4m3 and x_bf16 (other
+ * inputs take the GENERIC kernel); it reads W once for up to 16 tokens and
+ * once per 32 tokens above that (n = 17..32 in one pass: X is then converted
+ * by one extra small kernel per pass), the weights of a pass that another
+ * follows being left in L2.  Every output equals the single-token call's bit
+ * for bit, whatever n.  The other kernels take up to 16 tokens per pass (fewer
+ * when n * K is too large for shared memory), each pass re-reading W.
  * The tcgen05 path scales X by 2^-8 before its f16 conversion, so entries with
  * |x| >= 65520 * 2^8 (about 1.68e7) are out of range: they set the device
  * error word (nvfp4_device_error) and the output is not meaningful.
