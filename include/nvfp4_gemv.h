@@ -304,6 +304,15 @@ nvfp4_status nvfp4_quantize_bf16(const uint16_t *w_bf16, int N, int K, uint8_t *
  * when bit 8, 16 or 32 is set, else NVFP4_OK. */
 nvfp4_status nvfp4_device_error(cudaStream_t stream, int *code);
 
+/* Self-test of the failure path (no fault involved): enqueues on `stream` one
+ * kernel whose single thread waits on a shared-memory barrier phase that
+ * nothing completes; like every wait in the library's kernels it gives up
+ * after about 2 s and sets bit 1 of the device error word, so that a later
+ * nvfp4_device_error returns NVFP4_ERR_DEVICE_TIMEOUT (and re-zeroes the
+ * workspaces) while the CUDA context stays usable.  Asynchronous; returns
+ * NVFP4_OK or NVFP4_ERR_CUDA. */
+nvfp4_status nvfp4_selftest_wait_timeout(cudaStream_t stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char *nvfp4_last_error(void);
 

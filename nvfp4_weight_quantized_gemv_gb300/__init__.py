@@ -36,7 +36,8 @@ TILING_NAMES = {0: "auto", 1: "one_pass", 2: "greedy_321"}
 EXPORTS = ("nvfp4_gemv_batched", "nvfp4_gemv_batched_ex", "nvfp4_gemv_batched_noalloc",
            "nvfp4_gemv_swiglu", "nvfp4_ffn_swiglu", "nvfp4_moe_gemv_grouped",
            "nvfp4_gemv_workspace_size", "nvfp4_gemv_plan",
-           "nvfp4_quantize_ref", "nvfp4_quantize", "nvfp4_quantize_bf16", "nvfp4_device_error", "nvfp4_last_error", "nvfp4_version")
+           "nvfp4_quantize_ref", "nvfp4_quantize", "nvfp4_quantize_bf16", "nvfp4_device_error",
+           "nvfp4_selftest_wait_timeout", "nvfp4_last_error", "nvfp4_version")
 
 
 class Nvfp4Error(RuntimeError):
@@ -70,6 +71,8 @@ def lib():
                                    "`python -m nvfp4_weight_quantized_gemv_gb300.buildlib`")
             L = ctypes.CDLL(LIB_PATH)
             vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            L.nvfp4_selftest_wait_timeout.argtypes = [vp]
+            L.nvfp4_selftest_wait_timeout.restype = i
             L.nvfp4_gemv_batched.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
             L.nvfp4_gemv_batched.restype = i
             L.nvfp4_gemv_batched_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp, ctypes.POINTER(nvfp4_gemv_opts)]
@@ -311,6 +314,12 @@ def nvfp4_device_error(stream=None) -> int:
     if st == NVFP4_ERR_DEVICE_TIMEOUT:
         raise Nvfp4Error(st, nvfp4_last_error())
     return code.value
+
+
+def nvfp4_selftest_wait_timeout(stream=None) -> None:
+    """Enqueue the bounded-wait self-test kernel (a wait that nothing ends; it
+    gives up after about 2 s and sets the device error word's timeout bit)."""
+    _check(lib().nvfp4_selftest_wait_timeout(_stream_handle(stream)))
 
 
 def build(force: bool = False) -> str:

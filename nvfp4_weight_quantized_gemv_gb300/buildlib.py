@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libnvfp4_gemv.so")
 SOURCES = ["gemv_stream.cu", "gemv_tc.cu", "gemv_generic.cu", "abi.cu", "quantize_host.cpp", "gemv_noalloc.cu",
-           "quantize_gpu.cu", "moe_gemv.cu", "moe_mma.cu"]
+           "quantize_gpu.cu", "moe_gemv.cu", "moe_mma.cu",
+           "selftest.cu"]
 HEADERS = ["ptx.cuh", "tcgen05.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -726,6 +726,18 @@ extern "C" nvfp4_status nvfp4_device_error(cudaStream_t stream, int *code) {
     return fail(NVFP4_ERR_DEVICE_TIMEOUT, "a kernel gave up waiting on a barrier (error word 0x%x)", word);
 }
 
+extern "C" nvfp4_status nvfp4_selftest_wait_timeout(cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    DeviceState *d = nullptr;
+    nvfp4_status st = device_state(dev, &d);
+    if (st != NVFP4_OK) return st;
+    if ((e = launch_selftest_wait_timeout(d->err_word, stream)) != cudaSuccess)
+        return cuda_fail(e, "self-test kernel launch");
+    return NVFP4_OK;
+}
+
 extern "C" const char *nvfp4_last_error(void) { return t_last_error.c_str(); }
 
 extern "C" int nvfp4_version(void) { return 100; }

@@ -112,6 +112,7 @@ cudaError_t launch_stream(int variant, const CUtensorMap &tw, const CUtensorMap 
 cudaError_t launch_generic(const GenericParams &p, cudaStream_t stream);
 cudaError_t stream_set_smem_limits(int smem_optin);
 cudaError_t device_error_word(unsigned **ptr);  // device address of the error word
+cudaError_t launch_selftest_wait_timeout(unsigned *err, cudaStream_t stream);  // selftest.cu
 
 // tcgen05 kernel (gemv_tc.cu): units of 128 rows x 256 k; T = 8 or 16 staged
 // tokens; an even number of weight stages.  K is cut into `groups` k-groups
