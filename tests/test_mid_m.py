@@ -1,7 +1,7 @@
 """GPU parity of the mid-M path (n = 17..64 tokens): the tcgen05 kernel with 32
 staged tokens, X converted once to f16 x 2^-8 and streamed per unit through a
-ring, up to 32 tokens per read of W (atlas #266 tile GEMM for the verify and
-prefill widths).
+ring, up to 32 tokens per read of W (the widths atlas #266 serves with its
+mid-M tile GEMM: verify and prefill batches).
 
 Tolerance as for the GEMV: |y_gpu - y_ref| <= 1e-2 * (|y_ref| + 1), y_ref the
 oracle's unrounded fp64 value.  The k-group partition is the one of n <= 16,
