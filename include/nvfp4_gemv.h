@@ -60,7 +60,9 @@ typedef enum nvfp4_variant {
     NVFP4_VARIANT_MMA = 1,      /* TMA ring + register dequant + mma.sync f16 tensor cores */
     NVFP4_VARIANT_SIMT = 2,     /* TMA ring + register dequant + fp32 CUDA-core FMAs */
     NVFP4_VARIANT_GENERIC = 3,  /* plain loads, any K % 16 == 0 and any alignment */
-    NVFP4_VARIANT_TC = 4        /* TMA ring + dequant into tensor memory + tcgen05.mma (default) */
+    NVFP4_VARIANT_TC = 4,       /* TMA ring + dequant into tensor memory + tcgen05.mma kind::f16 */
+    NVFP4_VARIANT_FP4 = 5       /* TMA ring straight into block-scaled tcgen05.mma kind::mxf4nvf4 (W as
+                                   stored, X as a 6-term NVFP4 expansion written by a small prep kernel) */
 } nvfp4_variant;
 
 /* Token tiling.  ONE_PASS streams W once for all n tokens (chunks of up to 16
@@ -82,6 +84,7 @@ typedef struct nvfp4_gemv_opts {
     size_t workspace_bytes;  /* size of `workspace` (see nvfp4_gemv_workspace_size); if nonzero (with or without
                                 `workspace`) the plan keeps its scratch within it: n > 16 then takes 16-token
                                 passes instead of 32-token ones when those need more */
+    int inflight;            /* FP4 kernel: most weight stages requested and not yet landed per CTA (0 = default) */
 } nvfp4_gemv_opts;
 
 /* Launch plan the library would use (for tests and benchmarks). */

@@ -27,9 +27,9 @@ NVFP4_ERR_WORKSPACE = 6
 NVFP4_ERR_DEVICE_INPUT = 7
 
 # nvfp4_variant / nvfp4_tiling
-VARIANT_AUTO, VARIANT_MMA, VARIANT_SIMT, VARIANT_GENERIC, VARIANT_TC = 0, 1, 2, 3, 4
+VARIANT_AUTO, VARIANT_MMA, VARIANT_SIMT, VARIANT_GENERIC, VARIANT_TC, VARIANT_FP4 = 0, 1, 2, 3, 4, 5
 TILING_AUTO, TILING_ONE_PASS, TILING_GREEDY_321 = 0, 1, 2
-VARIANT_NAMES = {0: "auto", 1: "mma", 2: "simt", 3: "generic", 4: "tc"}
+VARIANT_NAMES = {0: "auto", 1: "mma", 2: "simt", 3: "generic", 4: "tc", 5: "fp4"}
 TILING_NAMES = {0: "auto", 1: "one_pass", 2: "greedy_321"}
 
 # Names the C ABI exports (include/nvfp4_gemv.h).
@@ -48,7 +48,8 @@ class Nvfp4Error(RuntimeError):
 
 class nvfp4_gemv_opts(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("tiling", ctypes.c_int), ("num_ctas", ctypes.c_int),
-                ("stages", ctypes.c_int), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+                ("stages", ctypes.c_int), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("inflight", ctypes.c_int)]
 
 
 class nvfp4_gemv_plan_info(ctypes.Structure):
@@ -119,9 +120,10 @@ def _check(status: int):
         raise Nvfp4Error(status, nvfp4_last_error())
 
 
-def _opts(variant=0, tiling=0, num_ctas=0, stages=0, workspace=None):
+def _opts(variant=0, tiling=0, num_ctas=0, stages=0, workspace=None, inflight=0):
     o = nvfp4_gemv_opts()
     o.variant, o.tiling, o.num_ctas, o.stages = int(variant), int(tiling), int(num_ctas), int(stages)
+    o.inflight = int(inflight)
     if workspace is not None:
         o.workspace = workspace.data_ptr()
         o.workspace_bytes = workspace.numel() * workspace.element_size()
@@ -214,14 +216,14 @@ def nvfp4_moe_gemv_grouped(w_packed, w_scale, w_global_scale, x, expert_offsets,
 
 
 def nvfp4_gemv_batched_ex(w_packed, w_scale, w_global_scale, x, y=None, stream=None, variant=0, tiling=0,
-                          num_ctas=0, stages=0, workspace=None):
-    """nvfp4_gemv_batched with explicit variant / tiling / grid / ring depth / workspace."""
+                          num_ctas=0, stages=0, workspace=None, inflight=0):
+    """nvfp4_gemv_batched with explicit variant / tiling / grid / ring depth / workspace / stages in flight."""
     import torch
     if y is None:
         n = x.shape[0] if x.dim() == 2 else 1
         y = torch.empty((n, w_packed.shape[0]), dtype=torch.bfloat16, device=x.device)
     n, N, K = _gemv_args(w_packed, w_scale, w_global_scale, x, y)
-    o = _opts(variant, tiling, num_ctas, stages, workspace)
+    o = _opts(variant, tiling, num_ctas, stages, workspace, inflight)
     _check(lib().nvfp4_gemv_batched_ex(w_packed.data_ptr(), w_scale.data_ptr(), w_global_scale.data_ptr(),
                                        x.data_ptr(), y.data_ptr(), n, N, K, _stream_handle(stream),
                                        ctypes.byref(o)))

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libnvfp4_gemv.so")
-SOURCES = ["gemv_stream.cu", "gemv_tc.cu", "gemv_generic.cu", "abi.cu", "quantize_host.cpp", "gemv_noalloc.cu",
+SOURCES = ["gemv_stream.cu", "gemv_tc.cu", "gemv_fp4.cu", "gemv_generic.cu", "abi.cu", "quantize_host.cpp", "gemv_noalloc.cu",
            "quantize_gpu.cu", "moe_gemv.cu", "moe_mma.cu",
            "selftest.cu"]
 HEADERS = ["ptx.cuh", "tcgen05.cuh", "internal.h"]

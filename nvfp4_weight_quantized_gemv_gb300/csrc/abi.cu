@@ -79,6 +79,8 @@ static nvfp4_status device_state(int dev, DeviceState **out) {
             return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
         if ((e = tc_set_smem_limit(d.smem_optin)) != cudaSuccess)
             return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory, tcgen05 kernel)");
+        if ((e = f4_set_smem_limit(d.smem_optin)) != cudaSuccess)
+            return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory, block-scaled FP4 kernel)");
         if ((e = moe_set_smem_limit(d.smem_optin)) != cudaSuccess)
             return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory, grouped expert kernel)");
         if ((e = moe_mma_set_smem_limit(d.smem_optin)) != cudaSuccess)
@@ -194,6 +196,11 @@ struct Plan {
     size_t partial_bytes = 0, x16_bytes = 0;
     TcPartition part{};  // tcgen05 kernel: k-groups and their CTAs
     size_t counter_bytes = 0, ws_bytes = 0;
+    // block-scaled FP4 kernel: MMA columns of the widest pass, parts bound,
+    // and the workspace regions after the partial tiles
+    int f4_cols_max = 0, f4_max_seg = 0, f4_max_parts = 0, f4_inflight = 0;
+    bool f4_x_resident = false;
+    size_t f4_xq_offset = 0, f4_et_offset = 0;
 };
 
 // Largest k-group (unit columns) whose X for 16 tokens fits next to eight
@@ -272,6 +279,31 @@ static nvfp4_status tc_partition(int N, int K, int ctas, int smem_optin, TcParti
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Block-scaled FP4 kernel: stream-K over the row-block-major units of all of
+// K (CTA c takes units [c U / C, (c + 1) U / C)); returns the most row-block
+// segments of one CTA (its partial-tile slots) and the most parts of one row
+// block.
+static nvfp4_status f4_partition(int N, int K, int ctas, int *max_seg, int *max_parts) {
+    const long long KC = K / kTcUnitKHost, RB = (N + kUnitRows - 1) / kUnitRows, U = RB * KC;
+    if (RB * KC * (ctas + 1) >= (1ll << 40))
+        return fail(NVFP4_ERR_UNSUPPORTED, "N = %d, K = %d: too many units for the FP4 kernel", N, K);
+    int ms = 1, mp = 1;
+    for (long long c = 0; c < ctas; ++c) {
+        const long long u0 = c * U / ctas, u1 = (c + 1) * U / ctas;
+        if (u1 > u0) {
+            const int segs = (int)((u1 - 1) / KC - u0 / KC + 1);
+            if (segs > ms) ms = segs;
+        }
+    }
+    for (long long rb = 0; rb < RB; ++rb) {
+        const long long ca = ((rb * KC + 1) * ctas - 1) / U, cb = ((rb * KC + KC) * ctas - 1) / U;
+        if (cb - ca + 1 > mp) mp = (int)(cb - ca + 1);
+    }
+    *max_seg = ms;
+    *max_parts = mp;
+    return NVFP4_OK;
+}
+
 // Greedy 3/2/1 token tiling: tiles of 3, then one tile of 2 or 1.
 static std::vector<int> greedy_321(int n) {
     std::vector<int> t;
@@ -311,9 +343,14 @@ static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nv
     if (p.variant == kTc && !tc_ok)
         return fail(NVFP4_ERR_INVALID_ARG,
                     "the tcgen05 variant needs K %% 256 == 0 and 16-byte aligned w_packed, w_scale_e4m3 and x_bf16");
+    if (p.variant == kFp4 && !fast_ok)
+        return fail(NVFP4_ERR_INVALID_ARG,
+                    "the FP4 variant needs K %% 256 == 0 and 16-byte aligned w_packed, w_scale_e4m3 and x_bf16");
+    if (p.variant == kFp4 && K > kF4MaxK)
+        return fail(NVFP4_ERR_UNSUPPORTED, "the FP4 variant takes K <= %d", kF4MaxK);
     p.tiling = (o.tiling == NVFP4_TILING_AUTO) ? NVFP4_TILING_ONE_PASS : o.tiling;
 
-    int per_pass = p.variant == kTc ? tc_per_pass : kMaxTokensPerPass;
+    int per_pass = p.variant == kTc ? tc_per_pass : p.variant == kFp4 ? kF4MaxTokensPerPass : kMaxTokensPerPass;
     if (p.variant == kMma || p.variant == kSimt) {
         // largest token count whose X still leaves room for two ring stages
         const int room = smem_optin - stream_smem_bytes(2, 0, K);
@@ -326,7 +363,43 @@ static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nv
     } else {
         for (int left = n; left > 0; left -= per_pass) p.tiles.push_back(left < per_pass ? left : per_pass);
     }
-    if (p.variant != kGeneric) {
+    if (p.variant == kFp4) {
+        int max_tile = 0;
+        for (int t : p.tiles) max_tile = t > max_tile ? t : max_tile;
+        p.units = (long long)((N + kUnitRows - 1) / kUnitRows) * (K / kTcUnitKHost);
+        int ctas = o.num_ctas ? o.num_ctas : sms;
+        if (ctas < 1 || ctas > sms) return fail(NVFP4_ERR_INVALID_ARG, "num_ctas must be 0 or 1..%d", sms);
+        if ((long long)ctas > p.units) ctas = (int)p.units;
+        p.ctas = ctas;
+        nvfp4_status st = f4_partition(N, K, ctas, &p.f4_max_seg, &p.f4_max_parts);
+        if (st != NVFP4_OK) return st;
+        p.f4_cols_max = f4_cols(max_tile);
+        // leave room on the SM for one X-prep CTA of the next call beside the GEMV
+        const int limit = smem_optin - 4096;
+        const int KC = K / kTcUnitKHost;
+        // small X term blocks stay resident for the whole call (a few bulk
+        // copies per CTA instead of one per unit)
+        p.f4_x_resident = (long long)KC * f4_slot_bytes(p.f4_cols_max) <= kF4ResidentXMax &&
+                          f4_max_stages(p.f4_cols_max, limit, true, KC) >= 4;
+        const int max_stages = f4_max_stages(p.f4_cols_max, limit, p.f4_x_resident, KC);
+        if (max_stages < 2) return fail(NVFP4_ERR_UNSUPPORTED, "the FP4 kernel does not fit shared memory");
+        int stages = max_stages;
+        if (o.stages != 0) {
+            if (o.stages > max_stages)
+                return fail(NVFP4_ERR_INVALID_ARG, "stages = %d does not fit (max %d)", o.stages, max_stages);
+            stages = o.stages;
+        }
+        p.stages = stages;
+        p.f4_inflight = o.inflight > 0 ? o.inflight : kF4DefaultInflight;
+        p.smem = f4_smem_bytes(stages, p.f4_cols_max, p.f4_x_resident, KC);
+        const int RB = (N + kUnitRows - 1) / kUnitRows;
+        p.counter_bytes = ws_counter_bytes(sms, RB);
+        p.partial_bytes = (size_t)ctas * p.f4_max_seg * kUnitRows * 16 * sizeof(float);
+        p.f4_xq_offset = p.counter_bytes + ((p.partial_bytes + 255) & ~(size_t)255);
+        const size_t xq_bytes = (size_t)KC * f4_slot_bytes(p.f4_cols_max);
+        p.f4_et_offset = p.f4_xq_offset + ((xq_bytes + 255) & ~(size_t)255);
+        p.ws_bytes = p.f4_et_offset + 16 * kF4Terms * sizeof(float);
+    } else if (p.variant != kGeneric) {
         int max_tile = 0;
         for (int t : p.tiles) max_tile = t > max_tile ? t : max_tile;
         const int T = max_tile > 16 ? 32 : max_tile > 8 ? 16 : 8;
@@ -382,12 +455,12 @@ static nvfp4_status validate(const void *wp, const void *ws, const void *gs, con
 }
 
 static nvfp4_status validate_opts(const nvfp4_gemv_opts &o) {
-    if (o.variant < kAuto || o.variant > kTc) return fail(NVFP4_ERR_INVALID_ARG, "unknown variant %d", o.variant);
+    if (o.variant < kAuto || o.variant > kFp4) return fail(NVFP4_ERR_INVALID_ARG, "unknown variant %d", o.variant);
     if (o.tiling < NVFP4_TILING_AUTO || o.tiling > NVFP4_TILING_GREEDY_321)
         return fail(NVFP4_ERR_INVALID_ARG, "unknown tiling %d", o.tiling);
     if (o.num_ctas < 0) return fail(NVFP4_ERR_INVALID_ARG, "num_ctas = %d must be >= 0", o.num_ctas);
-    if (o.stages != 0 && (o.stages < 2 || o.stages > kMaxStages))
-        return fail(NVFP4_ERR_INVALID_ARG, "stages must be 0 or 2..%d", kMaxStages);
+    if (o.stages != 0 && (o.stages < 2 || o.stages > (o.variant == kFp4 ? kF4MaxStages : kMaxStages)))
+        return fail(NVFP4_ERR_INVALID_ARG, "stages must be 0 or 2..%d", o.variant == kFp4 ? kF4MaxStages : kMaxStages);
     if (o.workspace && (reinterpret_cast<uintptr_t>(o.workspace) & 255u) != 0)
         return fail(NVFP4_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     return NVFP4_OK;
@@ -416,7 +489,7 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
     Plan plan;
     if ((st = make_plan(n, N, K, fast_ok, o, d->sms, d->smem_optin, &plan)) != NVFP4_OK) return st;
 
-    if (swiglu && plan.variant != kTc)
+    if (swiglu && plan.variant != kTc && plan.variant != kFp4)
         return fail(NVFP4_ERR_UNSUPPORTED,
                     "the fused SwiGLU runs on the tcgen05 path only (K %% 256 == 0, 16-byte aligned inputs, variant "
                     "AUTO or TC)");
@@ -445,7 +518,7 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
         return st;
     }
     CUtensorMap tw, ts;
-    if (plan.variant == kTc) {
+    if (plan.variant == kTc || plan.variant == kFp4) {
         if ((st = encode_2d(&tw, wp, (uint64_t)K / 2, (uint64_t)N, 128, kUnitRows, CU_TENSOR_MAP_SWIZZLE_128B)) !=
             NVFP4_OK)
             return st;
@@ -453,6 +526,40 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
         return st;
     }
     if ((st = encode_2d(&ts, ws, (uint64_t)K / 16, (uint64_t)N, 16, kUnitRows)) != NVFP4_OK) return st;
+
+    if (plan.variant == kFp4) {
+        F4Params fp;
+        fp.gscale = gs;
+        fp.counters = static_cast<unsigned *>(work);
+        fp.partials = reinterpret_cast<float *>(static_cast<char *>(work) + plan.counter_bytes);
+        fp.xq = static_cast<uint8_t *>(work) + plan.f4_xq_offset;
+        fp.xs = reinterpret_cast<float *>(static_cast<char *>(work) + plan.f4_et_offset);
+        fp.err = d->err_word;
+        fp.N = N;
+        fp.K = K;
+        fp.KC = K / kTcUnitKHost;
+        fp.ctas = plan.ctas;
+        fp.row_blocks = (N + kUnitRows - 1) / kUnitRows;
+        fp.max_seg = plan.f4_max_seg;
+        fp.stages = plan.stages;
+        fp.swiglu = swiglu ? 1 : 0;
+        fp.inflight = plan.f4_inflight;
+        fp.x_resident = plan.f4_x_resident ? 1 : 0;
+        const size_t y_stride_f4 = swiglu ? (size_t)N / 2 : (size_t)N;
+        int t0 = 0;
+        for (int tn : plan.tiles) {
+            fp.y = y + (size_t)t0 * y_stride_f4;
+            fp.n = tn;
+            fp.cols = f4_cols(tn);
+            fp.w_keep = (t0 + tn < n) ? 1 : 0;  // the next pass re-reads W: from L2, not HBM
+            if ((e = launch_fp4(tw, ts, x + (size_t)t0 * K, fp,
+                                f4_smem_bytes(plan.stages, fp.cols, plan.f4_x_resident, fp.KC), stream)) !=
+                cudaSuccess)
+                return cuda_fail(e, "FP4 kernel launch");
+            t0 += tn;
+        }
+        return NVFP4_OK;
+    }
 
     StreamParams sp;
     sp.gscale = gs;

@@ -1,0 +1,903 @@
+// gemv_fp4.cu -- the block-scaled FP4 tensor-core path of the NVFP4 batched
+// GEMV: the weights go from HBM to the tensor core as they are stored (E2M1
+// codes plus one E4M3 scale per 16 k), with no dequantisation on CUDA cores.
+//
+// Computes Y[t, r] = g * sum_k X[t, k] * E2M1(W[r, k]) * E4M3(S[r, k/16]) for
+// n <= 16 tokens from ONE pass over W (atlas pull request #266, "What it
+// does": a tile of decode tokens reads the projection weight once; here the
+// tile is all n tokens).
+//
+// The tensor core's block-scaled FP4 MMA (tcgen05.mma kind::mxf4nvf4,
+// scale_vec::4X) multiplies E2M1 operands that each carry an E4M3 scale per
+// 16 k -- exactly NVFP4 -- so the weight operand is the stored W tile and the
+// weight scales are the stored S bytes.  The other operand must be E2M1 too,
+// so each bf16 activation row is written as a sum of J = 8 E2M1 terms
+// (fp4_xprep_kernel), each with one fp32 scale for the whole row:
+//
+//     x[k] ~= sum_j s_j * q_j[k],   s_0 = max|x| / 6,   s_j = s_{j-1} / 6,
+//
+// q_j the E2M1 code (nearest, ties to even) of what the earlier terms left,
+// r_j / s_j.  The grid's largest gap (4 to 6) is 2, so |r_{j+1}| <= s_j =
+// 6 s_{j+1}: no term saturates, and after eight terms the residual is at most
+// max|x| / 6^8 (1.5e-7 of the row's largest entry; measured on N(0,1), 1 % x20
+// outlier, 1e-6-scaled and log-normal rows the worst output error stayed
+// below 0.1 of the 1e-2 (|y| + 1) tolerance).  The tensor core sees the codes
+// with a unit block scale; each term occupies its own MMA column (token t,
+// term j -> column 8t + j) and the epilogue applies the s_j and sums a token's
+// terms in a fixed order (the smallest first), multiplies by g and rounds to
+// bf16.  Every token's arithmetic is the same whatever n (the columns of an
+// MMA are independent, the expansion is per token), so a batched call equals
+// n single-token calls bit for bit.
+//
+// Work split.  Units of 128 rows x 256 k (one 16 KB W tile, 128-byte swizzle,
+// plus the rows' 16 scale bytes); the persistent grid (one CTA per SM) takes
+// equal contiguous ranges of the row-block-major unit order (stream-K over all
+// of K).  A row block held whole by one CTA is finished there; the parts of a
+// split row block are written as fp32 tiles and the CTA that adds the last
+// part (an atomic count per row block, or a look at it when the others are
+// known to be in) sums them in CTA order and stores the row -- fixed order,
+// no second launch, no waiting on other CTAs.  A CTA processes the partial
+// row block at the end of its range first, so that its part is published
+// early.
+//
+// Warp roles (384 threads):
+//   warp 0     weight producer: TMA of the unit's W and S tiles into a ring of S
+//              stages, at most `inflight` stages requested and not yet landed
+//              (HBM stays busy without queueing in front of latency-bound
+//              loads); the ring fills before the wait for the kernel ahead.
+//   warp 10    X loader: after that wait, the X codes -- all unit columns
+//              at once when they fit in shared memory, else one unit column
+//              per stage.
+//   warps 1,11 MMA issuers, units alternating (one issuer above 64 columns):
+//              per unit four MMAs (K = 64 each, M = 128 weight rows, N = 8n
+//              rounded up to 16 columns, fp32 in tensor memory) into the
+//              issuer's accumulator of the row-block segment; the whole warp
+//              runs the loop and one elected lane issues.
+//   warps 2-5  scale-factor warps, one per tensor-memory lane quarter: the MMA
+//              reads row m's four scale bytes of a K = 64 step from lane m,
+//              column base + m / 32 (measured on sm_103a); a warp copies its
+//              rows' 16 S bytes with one tcgen05.st per unit as soon as the
+//              stage lands (X is not needed for this).
+//   warps 6-9  epilogue: per finished row-block segment, tcgen05.ld of the
+//              accumulators, the per-token sum of terms, then the bf16 store or
+//              the split-row protocol above.
+//
+// Programmatic dependent launch: the X-prep kernel lets this grid launch at
+// once; this grid streams weights before its griddepcontrol.wait and lets the
+// next kernel (the next call's X prep) launch right after its setup.  X codes,
+// the term scales, g, the workspace and Y are touched only after the wait.
+// Every wait is bounded (2 s of %globaltimer); a timeout sets the device error
+// word, skips the remaining work, waits (bounded) for the CTA's own copies and
+// MMAs, and frees the tensor memory.
+#include "internal.h"
+#include "ptx.cuh"
+#include "tcgen05.cuh"
+
+#include <cuda_bf16.h>
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kF4WBytes = kUnitRows * 128;      // 128 rows x 256 packed k
+constexpr int kF4SBytes = kUnitRows * 16;       // 128 rows x 16 scale bytes
+constexpr int kF4WarpProducer = 0;
+constexpr int kF4WarpIssuer = 1;
+constexpr int kF4WarpSf0 = 2;                   // warps 2..5
+constexpr int kF4WarpEpi0 = 6;                  // warps 6..9
+constexpr int kF4WarpXLoad = 10;                // X loader
+constexpr int kF4WarpIssuer1 = 11;              // second MMA issuer (f4_issuers(cols) == 2)
+constexpr int kF4Threads = 12 * 32;
+constexpr uint32_t kF4TmemCols = 512;
+constexpr int kF4SfCols = 16;                   // tensor-memory columns per stage: the weight scales
+constexpr int kF4XprepThreads = 256;
+constexpr int kF4XprepElems = kF4XprepThreads * 8;  // activations per X-prep CTA
+constexpr unsigned kF4ErrSmemBase = 64u;            // dynamic shared memory not 1024-byte aligned
+constexpr uint32_t kF4UnitScale = 0x38383838u;      // four E4M3 1.0: the X codes' block scale
+
+__device__ __forceinline__ void mma_fp4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                        uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+            d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor of kind::mxf4nvf4: A and B E2M1 (format 1 in bits
+// [7,10) and [10,13)), both K-major, N >> 3 in [17,23), scale type E4M3 (bit
+// 23 = 0), M >> 4 in [24,29), scale-factor ids 0, K = 64 (bit 31 = 0).
+__host__ __device__ constexpr uint32_t idesc_fp4(int M, int N) {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void bulk_load_f4(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                             uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// True in one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n .reg .b32 r;\n .reg .pred p;\n elect.sync r|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(pred));
+    return pred != 0;
+}
+
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Named barrier over `threads` threads that also ORs `v` over them: every
+// participant gets the same answer (so a bounded wait that gave up in one warp
+// makes all of them leave together and no named barrier is left unmatched).
+__device__ __forceinline__ bool named_sync_or(int id, int threads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+        " bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
+// Progress counters in shared memory, written with release and read with
+// acquire semantics (CTA scope): cheaper than an mbarrier wait when the
+// producer side is known to be ahead.
+__device__ __forceinline__ void st_release_smem(uint32_t addr, uint32_t v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_smem(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// One row's outputs for all n tokens (v[t] = token t's sum of terms, before
+// g): y = bf16(v g), or with swiglu the gated form of rows 2f / 2f + 1 held by
+// lanes 2i / 2i + 1 (every lane of the warp must call it).
+__device__ __forceinline__ void f4_store_row(const F4Params &p, const float (&v)[16], int row, float g) {
+    const int lane = threadIdx.x & 31;
+    if (!p.swiglu) {
+        if (row < p.N) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                if (t < p.n) {
+                    __nv_bfloat16 h = __float2bfloat16_rn(v[t] * g);
+                    p.y[(size_t)t * p.N + row] = *reinterpret_cast<uint16_t *>(&h);
+                }
+            }
+        }
+        return;
+    }
+    const int F = p.N >> 1;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+        const float a = v[t] * g;
+        const float up = __shfl_down_sync(0xffffffffu, a, 1);
+        if (t < p.n && (lane & 1) == 0 && row < p.N) {
+            const float h = a / (1.0f + expf(-a)) * up;
+            __nv_bfloat16 hv = __float2bfloat16_rn(h);
+            p.y[(size_t)t * F + (row >> 1)] = *reinterpret_cast<uint16_t *>(&hv);
+        }
+    }
+}
+
+// Part c (a CTA) of split row block rb for this thread's row r.
+__device__ __forceinline__ void f4_load_part(const F4Params &p, float (&part)[16], int c, int rb, int r,
+                                             long long U, int KC) {
+    const long long cu0 = (long long)c * U / p.ctas;
+    const int crb0 = (int)(cu0 / KC);
+    const float4 *src = reinterpret_cast<const float4 *>(p.partials + ((size_t)c * p.max_seg + (rb - crb0)) *
+                                                                         (kUnitRows * 16) + (size_t)r * 16);
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd) {
+        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (4 * qd < p.n) f = __ldcg(src + qd);
+        part[4 * qd] = f.x;
+        part[4 * qd + 1] = f.y;
+        part[4 * qd + 2] = f.z;
+        part[4 * qd + 3] = f.w;
+    }
+}
+
+// Sum of the parts of split row block rb for this thread's row r, in CTA
+// order ca..cb (fixed, so the result does not depend on which CTA adds it);
+// part `self` is `own`, the others come from the partial tiles.
+__device__ __forceinline__ void f4_sum_parts(const F4Params &p, float (&sum)[16], int ca, int cb, int self,
+                                             const float (&own)[16], int rb, int r, long long U, int KC) {
+    for (int c = ca; c <= cb; ++c) {
+        float part[16];
+        if (c == self) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) part[t] = own[t];
+        } else {
+            f4_load_part(p, part, c, rb, r, U, KC);
+        }
+#pragma unroll
+        for (int t = 0; t < 16; ++t) sum[t] = c == ca ? part[t] : sum[t] + part[t];
+    }
+}
+
+// Eight fp32 values -> eight E2M1 codes, value j in nibble j (the hardware
+// conversion puts its first operand in the high nibble).
+__device__ __forceinline__ uint32_t f4_cvt_e2m1x8(const float (&q)[8]) {
+    uint32_t out;
+    asm("{\n"
+        " .reg .b8 c0, c1, c2, c3;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 c0, %2, %1;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 c1, %4, %3;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 c2, %6, %5;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 c3, %8, %7;\n"
+        " mov.b32 %0, {c0, c1, c2, c3};\n"
+        "}\n"
+        : "=r"(out)
+        : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+    return out;
+}
+
+}  // namespace
+
+// Shared memory: the ring (W + S tiles, plus the unit column's X codes when
+// they are streamed), the resident X codes (all K / 256 unit columns) when not,
+// the barriers, then flags and the term scales.
+int f4_smem_bytes(int stages, int cols, bool x_resident, int KC) {
+    const int slot = f4_slot_bytes(cols), groups = (KC + kF4XGroup - 1) / kF4XGroup;
+    const int xbars = x_resident ? (groups > stages ? groups : stages) : stages;
+    return stages * (kF4XOffHost + (x_resident ? 0 : slot)) + (x_resident ? KC * slot : 0) +
+           8 * (3 * stages + xbars + 8) + kF4MiscBytes;
+}
+
+// TMEM: accumulators [issuer][segment buffer 2][f4_dstride(cols)] from column
+// 0, the X codes' unit scale (4 columns, in a group of 16), then kF4SfCols per
+// stage.
+int f4_max_stages(int cols, int smem_limit, bool x_resident, int KC) {
+    const int tmem_stages = ((int)kF4TmemCols - 2 * f4_issuers(cols) * f4_dstride(cols) - 16) / kF4SfCols;
+    int s = 2;
+    while (s + 1 <= tmem_stages && s + 1 <= kF4MaxStages && f4_smem_bytes(s + 1, cols, x_resident, KC) <= smem_limit)
+        ++s;
+    return f4_smem_bytes(s, cols, x_resident, KC) <= smem_limit ? s : 0;
+}
+
+// ------------------------------------------------------------------ X prep
+// Token t = blockIdx.y; this CTA expands activations [blockIdx.x * 2048,
+// + 2048) of it.  Every CTA of a token reads the whole row once (all loads in
+// flight together, one memory round trip) to find max |x| itself, so all of
+// them derive the same term scales without exchanging anything.
+template <int L>  // 16-byte loads per thread that cover a whole row: ceil(K / 2048) rounded up to 1, 2, 4, 8, 16
+__global__ void __maxnreg__(64) fp4_xprep_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ xq,
+                                                 float *__restrict__ xs, int K, int cols) {
+    griddep_launch_dependents();  // the GEMV may launch and start streaming its weights
+    griddep_wait();               // X may be the output of the kernel ahead of this one
+    const int t = blockIdx.y, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)t * K);
+    const int nvec = K / 8;  // <= L * 256
+    const int own = blockIdx.x * kF4XprepThreads + tid;  // this thread's vector of this CTA's slice
+    uint4 v[L];
+#pragma unroll
+    for (int j = 0; j < L; ++j) {
+        const int i = tid + j * kF4XprepThreads;
+        v[j] = i < nvec ? __ldg(xr + i) : make_uint4(0, 0, 0, 0);
+    }
+    const uint4 mine = own < nvec ? __ldg(xr + own) : make_uint4(0, 0, 0, 0);  // one of the above: same request
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < L; ++j) {
+        m = __vmaxu2(m, v[j].x & 0x7FFF7FFFu);
+        m = __vmaxu2(m, v[j].y & 0x7FFF7FFFu);
+        m = __vmaxu2(m, v[j].z & 0x7FFF7FFFu);
+        m = __vmaxu2(m, v[j].w & 0x7FFF7FFFu);
+    }
+    m = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __shared__ uint32_t wmax[kF4XprepThreads / 32];
+    if (lane == 0) wmax[wid] = m;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kF4XprepThreads / 32; ++w) m = max(m, wmax[w]);
+    // bf16 magnitude bits: >= 0x7F80 inf or NaN (the token's outputs become NaN)
+    const bool finite = m < 0x7F80u;
+    float sc[kF4Terms];  // s_0 = max|x| / 6, s_j = s_{j-1} / 6 (zero for an all-zero row)
+    sc[0] = finite ? __fdiv_rn(__uint_as_float(m << 16), 6.0f) : __int_as_float(0x7FC00000);
+#pragma unroll
+    for (int j = 1; j < kF4Terms; ++j) sc[j] = __fdiv_rn(sc[j - 1], 6.0f);
+    if (blockIdx.x == 0 && tid < kF4Terms) {
+#pragma unroll
+        for (int j = 0; j < kF4Terms; ++j)
+            if (tid == j) xs[t * kF4Terms + j] = sc[j];
+    }
+    const int k0 = own * 8;
+    if (k0 >= K) return;
+    float r[8];
+    {
+        const uint32_t w[4] = {mine.x, mine.y, mine.z, mine.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            r[2 * i] = __uint_as_float(w[i] << 16);
+            r[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+    const int kc = k0 >> 8, bo = (k0 & 255) >> 1;
+    uint8_t *const tile = xq + (size_t)kc * f4_slot_bytes(cols);
+#pragma unroll
+    for (int j = 0; j < kF4Terms; ++j) {
+        uint32_t codes = 0;
+        if (finite && sc[j] > 0.f) {
+            const float inv = __frcp_rn(sc[j]);
+            float q[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q[i] = r[i] * inv;
+            codes = f4_cvt_e2m1x8(q);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t h2 = e2m1x2_to_f16x2_rt(codes, i);
+                const float2 d = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+                r[2 * i] = fmaf(-d.x, sc[j], r[2 * i]);
+                r[2 * i + 1] = fmaf(-d.y, sc[j], r[2 * i + 1]);
+            }
+        }
+        const int c = t * kF4Terms + j;  // MMA column of (token, term): row c of the unit column's code tile
+        *reinterpret_cast<uint32_t *>(tile + c * 128 + ((((bo >> 4) ^ (c & 7)) << 4) | (bo & 15))) = codes;
+    }
+}
+
+// Processing order of a CTA's units.  The CTA's range [u0, u0 + count) of the
+// row-block-major order falls into `nseg` row-block segments (natural order);
+// when the last one is partial (a split row block continued by the next CTA)
+// it is processed first, so that this CTA's contribution to it is published
+// early and whichever CTA completes that row block does not wait on it.
+struct F4Order {
+    int rb0, kc0, count, KC, nseg;
+    bool rot;
+    __device__ void init(long long u0, int cnt, int kc) {
+        KC = kc;
+        count = cnt;
+        rb0 = (int)(u0 / KC);
+        kc0 = (int)(u0 - (long long)rb0 * KC);
+        nseg = cnt > 0 ? (int)((u0 + cnt - 1) / KC - u0 / KC + 1) : 0;
+        rot = nseg >= 2 && seg_len(nseg - 1) < KC;
+    }
+    __device__ int nat(int s) const { return rot ? (s == 0 ? nseg - 1 : s - 1) : s; }   // natural index
+    __device__ int seg_kc(int ns) const { return ns == 0 ? kc0 : 0; }                    // first unit column
+    __device__ int seg_len(int ns) const {
+        if (ns == 0) return min(KC - kc0, count);
+        const int before = (KC - kc0) + (ns - 1) * KC;
+        return min(KC, count - before);
+    }
+};
+
+// Walks the units in processing order (row block, unit column) together with
+// their ring stage and its phase parity; everything held in registers (no
+// pointer to the order, no division per unit).
+struct F4Walk {
+    F4Order o;
+    int s, ns, rb, kc, left;
+    int st, S;          // ring stage of the current unit, ring size
+    unsigned ph;        // parity of the stage's current phase
+    __device__ void begin(const F4Order &ord, int stages) {
+        o = ord;
+        S = stages;
+        s = 0;
+        st = 0;
+        ph = 0;
+        if (o.nseg > 0) enter();
+    }
+    __device__ void enter() {
+        ns = o.nat(s);
+        rb = o.rb0 + ns;
+        kc = o.seg_kc(ns);
+        left = o.seg_len(ns);
+    }
+    __device__ void next() {  // advance by one unit
+        ++kc;
+        if (++st == S) {
+            st = 0;
+            ph ^= 1u;
+        }
+        if (--left == 0 && ++s < o.nseg) enter();
+    }
+};
+
+// ------------------------------------------------------------------- GEMV
+template <int NC>  // MMA columns: 16 * ceil(8 n / 16)
+__global__ void __maxnreg__(128)
+    gemv_fp4_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
+                    const F4Params p) {
+    static_assert(NC % 16 == 0 && NC >= 16 && NC <= kF4MaxCols, "columns");
+    constexpr int kDStride = NC <= 32 ? 32 : NC <= 64 ? 64 : 128;
+    constexpr int kIssuers = NC <= 64 ? 2 : 1;  // units alternate between the issuers (own accumulators)
+    constexpr uint32_t kSlot = 128u * NC;       // one unit column's X codes
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t sbase = smem_u32(smem_raw);
+    if (sbase & 1023u) {  // the swizzled tiles need a 1024-byte aligned base; never expected
+        griddep_wait();
+        if (threadIdx.x == 0) atomicOr(p.err, kF4ErrSmemBase);
+        return;
+    }
+    const int S = p.stages;
+    const int KC = p.KC;
+    const bool xres = p.x_resident != 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- this CTA's unit range and the order it processes them in
+    const long long U = (long long)p.row_blocks * KC;
+    const long long u0 = (long long)blockIdx.x * U / p.ctas;
+    const int count = (int)((long long)(blockIdx.x + 1) * U / p.ctas - u0);
+    F4Order ord;
+    ord.init(u0, count, KC);
+
+    // ---- shared memory: ring stages [W 16 KB][S 2 KB]([X slot] when streamed),
+    // resident X slots [KC] when not, then the barriers
+    const uint32_t kStage = kF4XOffHost + (xres ? 0u : kSlot);
+    const uint32_t sX = sbase + S * kStage;                  // resident X codes
+    const int xgroups = (KC + kF4XGroup - 1) / kF4XGroup;    // bulk copies of resident X codes
+    const int xbars = xres ? (xgroups > S ? xgroups : S) : S;
+    const uint32_t sFull = sX + (xres ? KC * kSlot : 0u);    // [S] W + S landed (TMA)
+    const uint32_t sXFull = sFull + 8 * S;      // [S] X codes of the stage landed / [xgroups] resident groups landed
+    const uint32_t sSf = sXFull + 8 * xbars;    // [S] weight scales in tensor memory, count 4
+    const uint32_t sEmpty = sSf + 8 * S;        // [S] MMAs done with the stage (commit)
+    const uint32_t sDFull = sEmpty + 8 * S;     // [issuer][2] segment accumulated (commit)
+    const uint32_t sDEmpty = sDFull + 32;       // [2] accumulators read, count 4
+    const uint32_t sFinal = sDEmpty + 16;       // [issuer] every MMA done (commit)
+    const uint32_t sMisc = sFinal + 16;         // [0] tensor-memory base, [1] last-part flag, [2] preload flag,
+                                                // [4 + q] units whose weight scales quarter q has stored
+    uint32_t *const misc = reinterpret_cast<uint32_t *>(smem_raw + (sMisc - sbase));
+    const uint32_t sSfDone = sMisc + 16;
+    float *const tscale = reinterpret_cast<float *>(misc + 8);  // [16][kF4Terms] the tokens' term scales
+    // X codes of the unit with unit column kc in stage st
+    auto x_addr = [&](int st, int kc) -> uint32_t {
+        return xres ? sX + (uint32_t)kc * kSlot : sbase + (uint32_t)st * kStage + kF4XOffHost;
+    };
+
+    // Weights are read once per call: evict-first, unless another pass over
+    // the same weights follows (n > 16), which keeps them in L2.
+    const uint64_t w_policy = p.w_keep ? l2_policy_evict_last() : l2_policy_evict_first();
+    F4Walk wk{};  // the producer's walk
+    auto issue_w = [&]() {
+        const uint32_t stage = sbase + wk.st * kStage, full = sFull + 8 * wk.st;
+        mbar_arrive_expect_tx(full, kF4WBytes + kF4SBytes);
+        tma_load_2d(stage, &tmap_w, wk.kc * 128, wk.rb * kUnitRows, full, w_policy);
+        tma_load_2d(stage + kF4WBytes, &tmap_s, wk.kc * 16, wk.rb * kUnitRows, full, w_policy);
+        wk.next();
+    };
+    // The weight stream: at most `inflight` stages requested and not yet
+    // landed, so that HBM stays busy without queueing so much in front of the
+    // latency-bound loads (X, partial tiles) that they wait microseconds.
+    const int inflight = p.inflight < S ? p.inflight : S;
+    const int pre = count < inflight ? count : inflight;
+    int issued = 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(sFull + 8 * s, 1);
+            mbar_init(sSf + 8 * s, 4);
+            mbar_init(sEmpty + 8 * s, 1);
+        }
+        for (int s = 0; s < xbars; ++s) mbar_init(sXFull + 8 * s, 1);
+        for (int b = 0; b < 4; ++b) mbar_init(sDFull + 8 * b, 1);
+        for (int b = 0; b < 2; ++b) mbar_init(sDEmpty + 8 * b, 4);
+        for (int b = 0; b < 2; ++b) mbar_init(sFinal + 8 * b, 1);
+        for (int q = 0; q < 4; ++q) misc[4 + q] = 0;
+        fence_barrier_init();
+        if (count > 0) wk.begin(ord, S);
+        for (; issued < pre; ++issued) issue_w();
+    }
+    if (warp == kF4WarpIssuer) {
+        tc::tmem_alloc(sMisc, kF4TmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tbase = misc[0];
+    // the next kernel on the stream (the next call's X prep) may launch now
+    if (threadIdx.x == 0) griddep_launch_dependents();
+    const uint32_t sfb = tbase + 2 * kIssuers * kDStride;  // the X codes' unit block scale
+    const uint32_t sfa_base = sfb + 16;                     // weight scales: kF4SfCols columns per stage
+
+    if (warp == kF4WarpProducer) {
+        // ---------------------------------------------------- weight producer
+        if (lane == 0) {
+            int lst = 0;       // stage of unit issued - inflight, whose landing paces the stream
+            unsigned lph = 0;  // and its parity
+            for (; issued < count; ++issued) {
+                if ((issued >= S && !mbar_wait_bounded(sEmpty + 8 * wk.st, wk.ph ^ 1u)) ||
+                    !mbar_wait_bounded(sFull + 8 * lst, lph)) {
+                    atomicOr(p.err, kDevErrTimeoutEmpty);
+                    break;
+                }
+                issue_w();
+                if (++lst == S) {
+                    lst = 0;
+                    lph ^= 1u;
+                }
+            }
+            // wait (bounded) for the most recent copies into every stage before exiting
+            const int lo = issued > S ? issued - S : 0;
+            for (int i = lo; i < issued; ++i) {
+                if (!mbar_wait_bounded(sFull + 8 * (i % S), (i / S) & 1)) {
+                    atomicOr(p.err, kDevErrTimeoutDrain);
+                    break;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kF4WarpXLoad) {
+        // ----------------------------------------------------------- X loader
+        if (lane == 0 && count > 0) {
+            griddep_wait();  // the X codes are the output of the X-prep kernel ahead
+            const uint64_t x_policy = l2_policy_evict_last();  // every CTA reads the same X codes
+            if (xres) {
+                // every unit column's X codes, kF4XGroup columns per bulk copy
+                for (int g = 0; g < xgroups; ++g) {
+                    const int c0 = g * kF4XGroup, nc = KC - c0 < kF4XGroup ? KC - c0 : kF4XGroup;
+                    const uint32_t bytes = (uint32_t)nc * kSlot, bar = sXFull + 8 * g;
+                    mbar_arrive_expect_tx(bar, bytes);
+                    bulk_load_f4(sX + (uint32_t)c0 * kSlot, p.xq + (size_t)c0 * kSlot, bytes, bar, x_policy);
+                }
+                for (int g = 0; g < xgroups; ++g) {
+                    if (!mbar_wait_bounded(sXFull + 8 * g, 0)) {
+                        atomicOr(p.err, kDevErrTimeoutDrain);
+                        break;
+                    }
+                }
+            } else {
+                F4Walk xw;
+                xw.begin(ord, S);
+                int loaded = 0;
+                for (; loaded < count; ++loaded) {
+                    if (loaded >= S && !mbar_wait_bounded(sEmpty + 8 * xw.st, xw.ph ^ 1u)) {
+                        atomicOr(p.err, kDevErrTimeoutEmpty);
+                        break;
+                    }
+                    const uint32_t bar = sXFull + 8 * xw.st;
+                    mbar_arrive_expect_tx(bar, kSlot);
+                    bulk_load_f4(sbase + xw.st * kStage + kF4XOffHost, p.xq + (size_t)xw.kc * kSlot, kSlot, bar,
+                                 x_policy);
+                    xw.next();
+                }
+                const int lo = loaded > S ? loaded - S : 0;
+                for (int i = lo; i < loaded; ++i) {
+                    if (!mbar_wait_bounded(sXFull + 8 * (i % S), (i / S) & 1)) {
+                        atomicOr(p.err, kDevErrTimeoutDrain);
+                        break;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kF4WarpIssuer || (kIssuers == 2 && warp == kF4WarpIssuer1)) {
+        // ------------------------------------------------------------- issuers
+        // Issuer j takes the units i with i % kIssuers == j, into its own
+        // accumulator per segment buffer.  The whole warp runs the loop (the
+        // descriptors stay warp-uniform) and one elected lane issues: much
+        // cheaper per MMA than a single lane on its own.
+        const int j = warp == kF4WarpIssuer ? 0 : 1;
+        constexpr uint32_t idesc = idesc_fp4(kUnitRows, NC);
+        // descriptors at shared address 0; the operand's address goes into the
+        // start field (bits [0, 14), 16-byte units; no carry below 256 KB)
+        const uint64_t desc0 = tc::smem_desc_sw128(0, 1024);
+        bool ok = true;
+        int mine = 0;          // the current unit's issuer (units alternate)
+        int i = 0;             // the current unit's index in processing order
+        int sf_known = 0;      // units whose weight scales are known to be in tensor memory
+        uint32_t xg_ready = 0; // resident X code groups known to have landed (bit per group)
+        F4Walk iw;
+        if (count > 0) iw.begin(ord, S);
+        for (int s = 0; s < ord.nseg && ok; ++s) {
+            const int len = iw.left;
+            const int sb = s & 1;
+            if (s >= 2 && __any_sync(0xffffffffu, !mbar_wait_bounded(sDEmpty + 8 * sb, ((s >> 1) - 1) & 1))) {
+                ok = false;
+                break;
+            }
+            const uint32_t d_tmem = tbase + (j * 2 + sb) * kDStride;
+            bool first = true;
+            for (int u = 0; u < len; ++u, ++i, iw.next(), mine = kIssuers == 2 ? mine ^ 1 : 0) {
+                if (mine != j) continue;
+                const int st = iw.st;
+                // the unit's weight scales: the scale-factor warps run ahead, so
+                // their progress counters usually say so without a wait
+                bool good = true;
+                if (sf_known <= i) {
+                    uint32_t lo = ld_acquire_smem(sSfDone);
+#pragma unroll
+                    for (int q = 1; q < 4; ++q) lo = min(lo, ld_acquire_smem(sSfDone + 4 * q));
+                    sf_known = (int)lo;
+                    if (sf_known <= i) good = mbar_wait_bounded(sSf + 8 * st, iw.ph);
+                }
+                // the unit's X codes: resident ones are waited for once per group
+                if (xres) {
+                    const int xg = iw.kc / kF4XGroup;
+                    if (!((xg_ready >> xg) & 1u)) {
+                        good = good && mbar_wait_bounded(sXFull + 8 * xg, 0);
+                        xg_ready |= 1u << xg;
+                    }
+                } else {
+                    good = good && mbar_wait_bounded(sXFull + 8 * st, iw.ph);
+                }
+                if (__any_sync(0xffffffffu, !good)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint64_t ad = desc0 + ((sbase + st * kStage) >> 4), bd = desc0 + (x_addr(st, iw.kc) >> 4);
+                const uint32_t sfa = sfa_base + st * kF4SfCols;
+                __syncwarp();
+                if (elect_one()) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_fp4(d_tmem, ad + 2 * k, bd + 2 * k, idesc, sfa + 4 * k, sfb, (!first || k > 0) ? 1u : 0u);
+                    tc::commit(sEmpty + 8 * st);
+                }
+                __syncwarp();
+                first = false;
+            }
+            // every segment is closed by both issuers, so the epilogue sees each phase
+            if (elect_one()) tc::commit(sDFull + 8 * (j * 2 + sb));
+            __syncwarp();
+        }
+        if (lane == 0) {
+            if (!ok) atomicOr(p.err, kDevErrTimeoutFull);
+            tc::commit(sFinal + 8 * j);
+            if (!mbar_wait_bounded(sFinal + 8 * j, 0)) atomicOr(p.err, kDevErrTimeoutDrain);
+        }
+        __syncwarp();
+    } else if (warp >= kF4WarpSf0 && warp < kF4WarpEpi0) {
+        // ------------------------------------------------- scale-factor warps
+        // Lane quarter q: rows 32q + lane.  Per stage, kF4SfCols columns: the
+        // MMA of step s reads column 4s + q for its quarter-q rows, so every
+        // column of the group gets the word.  First the X codes' unit scale:
+        // four columns of E4M3 1.0 that every MMA reads (column n / 32 for
+        // token-term column n), the same in every quarter.
+        const int q = warp & 3;
+        const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
+        const int r = 32 * q + lane;
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%1,%1,%1};" ::"r"(sfb + lane_bits),
+                     "r"(kF4UnitScale)
+                     : "memory");
+        bool ok = true;
+        F4Walk sw;
+        if (count > 0) sw.begin(ord, S);
+        for (int i = 0; i < count; ++i, sw.next()) {
+            const int st = sw.st;
+            if (__any_sync(0xffffffffu, !mbar_wait_bounded(sFull + 8 * st, sw.ph))) {
+                ok = false;
+                break;
+            }
+            const uint4 a = lds128(sbase + st * kStage + kF4WBytes + 16 * r);
+            const uint32_t v[16] = {a.x, a.x, a.x, a.x, a.y, a.y, a.y, a.y, a.z, a.z, a.z, a.z, a.w, a.w, a.w, a.w};
+            tc::st_32x32b_x16(sfa_base + lane_bits + st * kF4SfCols, v);
+            tc::wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(sSf + 8 * st);
+                st_release_smem(sSfDone + 4 * q, (uint32_t)(i + 1));
+            }
+        }
+        tc::wait_st();
+        if (!ok && lane == 0) atomicOr(p.err, kDevErrTimeoutFull);
+    } else if (warp >= kF4WarpEpi0 && warp < kF4WarpEpi0 + 4) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
+        const int r = 32 * q + lane;
+        griddep_wait();  // the term scales, g, the workspace and Y belong to this call from here on
+        const float g = __ldg(p.gscale);
+        for (int i = (int)threadIdx.x - kF4WarpEpi0 * 32; i < 16 * kF4Terms; i += 128)
+            tscale[i] = i < p.n * kF4Terms ? __ldcg(p.xs + i) : 0.f;
+        named_sync(1, 128);
+        // the other part of a two-part row block, loaded ahead of time
+        float pre_part[16];
+        int pre_rb = -1;
+        int seg_i0 = 0;  // processing-order index of the segment's first unit
+        for (int s = 0; s < ord.nseg; seg_i0 += ord.seg_len(ord.nat(s)), ++s) {
+            const int ns = ord.nat(s);
+            const int rb = ord.rb0 + ns;
+            const int len = ord.seg_len(ns);
+            const bool whole = len == KC;
+            const long long ub = (long long)rb * KC;
+            const int ca = (int)(((ub + 1) * p.ctas - 1) / U), cb = (int)(((ub + KC) * p.ctas - 1) / U);
+            // Before the last segment's accumulator is ready: if it is one of the
+            // two parts of a split row block and the other part is already
+            // published, load that now; this CTA then adds the last part and
+            // needs no count (a two-part sum is the same in either order).
+            if (s == ord.nseg - 1 && !whole && cb == ca + 1) {
+                if (warp == kF4WarpEpi0 && lane == 0) misc[2] = ld_acquire_u32(p.counters + rb) == 1u ? 1u : 0u;
+                named_sync(1, 128);
+                if (misc[2]) {
+                    pre_rb = rb;
+                    f4_load_part(p, pre_part, (int)blockIdx.x == ca ? cb : ca, rb, r, U, KC);
+                }
+            }
+            const int sb = s & 1;
+            bool waited = true;
+#pragma unroll
+            for (int j = 0; j < kIssuers; ++j)
+                waited = waited && mbar_wait_bounded(sDFull + 8 * (j * 2 + sb), (s >> 1) & 1);
+            // all four epilogue warps leave together if any of them gave up
+            if (named_sync_or(1, 128, !waited)) {
+                if (lane == 0) atomicOr(p.err, kDevErrTimeoutFull);
+                break;
+            }
+            tc::fence_after_sync();
+            // issuer j contributed to this segment if one of its units lies in it
+            const bool from1 = kIssuers == 2 && (len >= 2 || (seg_i0 & 1) == 1);
+            const bool from0 = kIssuers == 1 || len >= 2 || (seg_i0 & 1) == 0;
+            float acc[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) acc[t] = 0.f;
+            // columns in chunks of 32 (four tokens' eight terms)
+#pragma unroll
+            for (int c0 = 0; c0 < NC; c0 += 32) {
+                uint32_t d[32];
+                // the issuers' accumulators, summed in issuer order
+#pragma unroll
+                for (int c = 0; c < 32; c += 16) {
+                    if (c0 + c < NC) {
+                        uint32_t part[16];
+                        tc::ld_32x32b_x16(tbase + lane_bits + ((from0 ? 0 : 2) + sb) * kDStride + c0 + c, part);
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) d[c + jj] = part[jj];
+                    }
+                }
+                tc::wait_ld();
+                if (kIssuers == 2 && from0 && from1) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 16) {
+                        if (c0 + c < NC) {
+                            uint32_t part[16];
+                            tc::ld_32x32b_x16(tbase + lane_bits + (2 + sb) * kDStride + c0 + c, part);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj)
+                                d[c + jj] = __float_as_uint(__uint_as_float(d[c + jj]) + __uint_as_float(part[jj]));
+                        }
+                    }
+                }
+#pragma unroll
+                for (int tl = 0; tl < 4; ++tl) {
+                    const int t = c0 / kF4Terms + tl;
+                    if (t < 16 && c0 + kF4Terms * tl + kF4Terms - 1 < NC) {
+                        // the terms times their scales, the smallest first
+                        float sum = __uint_as_float(d[kF4Terms * tl + kF4Terms - 1]) *
+                                    tscale[t * kF4Terms + kF4Terms - 1];
+#pragma unroll
+                        for (int jj = kF4Terms - 2; jj >= 0; --jj)
+                            sum = sum + __uint_as_float(d[kF4Terms * tl + jj]) * tscale[t * kF4Terms + jj];
+                        acc[t] = sum;
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sDEmpty + 8 * sb);
+            const int row = rb * kUnitRows + r;
+            if (whole) {
+                f4_store_row(p, acc, row, g);
+                continue;
+            }
+            // A split row block.  This CTA adds the last part when the other
+            // parts are in already -- found before the segment (and loaded
+            // ahead, two-part rows) or now (loaded now) -- or when its count
+            // arrives last; it then sums the parts in CTA order.  Otherwise it
+            // publishes its part and counts it.
+            bool last = pre_rb == rb, loaded = last;
+            if (!last) {
+                if (warp == kF4WarpEpi0 && lane == 0)
+                    misc[2] = ld_acquire_u32(p.counters + rb) + 1 == (unsigned)(cb - ca + 1) ? 1u : 0u;
+                named_sync(1, 128);
+                last = misc[2] != 0;
+            }
+            if (!last) {
+                float *const part_out =
+                    p.partials + ((size_t)blockIdx.x * p.max_seg + ns) * (kUnitRows * 16) + (size_t)r * 16;
+#pragma unroll
+                for (int qd = 0; qd < 4; ++qd)
+                    if (4 * qd < p.n)
+                        __stcg(reinterpret_cast<float4 *>(part_out) + qd,
+                               make_float4(acc[4 * qd], acc[4 * qd + 1], acc[4 * qd + 2], acc[4 * qd + 3]));
+                __threadfence();
+                named_sync(1, 128);
+                if (warp == kF4WarpEpi0 && lane == 0) {
+                    const unsigned old = atomicAdd(p.counters + rb, 1u);
+                    misc[1] = (old + 1 == (unsigned)(cb - ca + 1)) ? 1u : 0u;
+                }
+                named_sync(1, 128);
+                last = misc[1] != 0;
+                if (last) __threadfence();
+            }
+            if (!last) continue;
+            float sum[16];
+            if (loaded) {
+                // the two parts of the row block; either order gives the same sum
+#pragma unroll
+                for (int t = 0; t < 16; ++t) sum[t] = acc[t] + pre_part[t];
+            } else {
+                f4_sum_parts(p, sum, ca, cb, (int)blockIdx.x, acc, rb, r, U, KC);
+            }
+            f4_store_row(p, sum, row, g);
+            if (warp == kF4WarpEpi0 && lane == 0) p.counters[rb] = 0;  // ready for the next call
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == kF4WarpIssuer) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tbase, kF4TmemCols);
+    }
+}
+
+cudaError_t f4_set_smem_limit(int smem_optin) {
+    cudaError_t e;
+#define NVFP4_F4_SET(NCV)                                                                                     \
+    if ((e = cudaFuncSetAttribute(gemv_fp4_kernel<NCV>, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
+                                  smem_optin)) != cudaSuccess)                                                \
+        return e;
+    NVFP4_F4_SET(16)
+    NVFP4_F4_SET(32)
+    NVFP4_F4_SET(48)
+    NVFP4_F4_SET(64)
+    NVFP4_F4_SET(80)
+    NVFP4_F4_SET(96)
+    NVFP4_F4_SET(112)
+    NVFP4_F4_SET(128)
+#undef NVFP4_F4_SET
+    return cudaSuccess;
+}
+
+cudaError_t launch_fp4(const CUtensorMap &tw, const CUtensorMap &ts, const uint16_t *x, const F4Params &p, int smem,
+                       cudaStream_t stream) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t xc = {};
+    xc.gridDim = dim3((unsigned)((p.K + kF4XprepElems - 1) / kF4XprepElems), (unsigned)p.n);
+    xc.blockDim = dim3(kF4XprepThreads);
+    xc.stream = stream;
+    xc.attrs = attr;
+    xc.numAttrs = 1;
+    const int loads = (p.K + kF4XprepElems - 1) / kF4XprepElems;
+    cudaError_t e;
+    if (loads <= 1) e = cudaLaunchKernelEx(&xc, fp4_xprep_kernel<1>, x, p.xq, p.xs, p.K, p.cols);
+    else if (loads <= 2) e = cudaLaunchKernelEx(&xc, fp4_xprep_kernel<2>, x, p.xq, p.xs, p.K, p.cols);
+    else if (loads <= 4) e = cudaLaunchKernelEx(&xc, fp4_xprep_kernel<4>, x, p.xq, p.xs, p.K, p.cols);
+    else if (loads <= 8) e = cudaLaunchKernelEx(&xc, fp4_xprep_kernel<8>, x, p.xq, p.xs, p.K, p.cols);
+    else e = cudaLaunchKernelEx(&xc, fp4_xprep_kernel<16>, x, p.xq, p.xs, p.K, p.cols);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.ctas);
+    cfg.blockDim = dim3(kF4Threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    switch (p.cols) {
+        case 16: return cudaLaunchKernelEx(&cfg, gemv_fp4_kernel<16>, tw, ts, p);
+        case 32: return cudaLaunchKernelEx(&cfg, gemv_fp4_kernel<32>, tw, ts, p);
+        case 48: return cudaLaunchKernelEx(&cfg, gemv_fp4_kernel<48>, tw, ts, p);
+        case 64: return cudaLaunchKernelEx(&cfg, gemv_fp4_kernel<64>, tw, ts, p);
+        case 80: return cudaLaunchKernelEx(&cfg, gemv_fp4_kernel<80>, tw, ts, p);
+        case 96: return cudaLaunchKernelEx(&cfg, gemv_fp4_kernel<96>, tw, ts, p);
+        case 112: return cudaLaunchKernelEx(&cfg, gemv_fp4_kernel<112>, tw, ts, p);
+        case 128: return cudaLaunchKernelEx(&cfg, gemv_fp4_kernel<128>, tw, ts, p);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace nvfp4

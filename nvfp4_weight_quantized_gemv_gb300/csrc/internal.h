@@ -24,7 +24,7 @@ constexpr int kTcMaxTokensPerPass = 32;  // tcgen05 kernel with the X ring
 constexpr int kSlotFloats = 32 * 16;  // one warp's partial tile: 32 lanes x 16 fp32
 constexpr int kCountersPerCta = 8;    // split-tile counters per CTA (one per fixup warp)
 
-enum Variant : int { kAuto = 0, kMma = 1, kSimt = 2, kGeneric = 3, kTc = 4 };
+enum Variant : int { kAuto = 0, kMma = 1, kSimt = 2, kGeneric = 3, kTc = 4, kFp4 = 5 };
 
 struct StreamParams {
     const uint16_t *x;   // [n][K] bf16, 16-byte aligned
@@ -41,6 +41,51 @@ struct StreamParams {
     int swiglu;          // tcgen05 only: rows 2f, 2f+1 are gate_f, up_f; y is h[n][N/2] = silu(gate) * up
     int w_keep;          // tcgen05 only: another pass over the same weights follows (keep them in L2)
 };
+
+// Block-scaled FP4 tensor-core path (gemv_fp4.cu).  Per pass of up to 16
+// tokens: fp4_xprep_kernel writes each token's activations as kF4Terms E2M1
+// terms with one fp32 scale per (token, term) -- MMA columns 8t + j -- into
+// the workspace, then the GEMV streams the stored W and S tiles straight into
+// tcgen05.mma kind::mxf4nvf4.  Workspace per unit column of 256 k: the codes
+// [cols][128 B] (128-byte swizzled rows); the scales [16][kF4Terms] floats.
+constexpr int kF4Terms = 8;
+constexpr int kF4MaxTokensPerPass = 16;
+constexpr int kF4MaxCols = 128;              // 16 tokens x 8 terms
+constexpr int kF4MaxStages = 16;
+constexpr int kF4XOffHost = 16384 + 2048;    // X codes inside a ring stage, after the W and S tiles
+constexpr int kF4MaxK = 32768;               // the X-prep kernel reads a whole row in one round of loads
+constexpr int kF4DefaultInflight = 4;
+constexpr int kF4MiscBytes = 32 + 16 * kF4Terms * 4 + 64;  // flags and counters, the term scales, slack
+inline int f4_cols(int n) { return 16 * ((n * kF4Terms + 15) / 16); }
+#ifdef __CUDACC__
+#define NVFP4_HD __host__ __device__
+#else
+#define NVFP4_HD
+#endif
+NVFP4_HD inline int f4_slot_bytes(int cols) { return 128 * cols; }  // one unit column's X codes
+constexpr int kF4XGroup = 4;                 // unit columns per bulk copy of resident X codes
+constexpr int kF4ResidentXMax = 112 * 1024;  // largest X code block kept resident in shared memory
+inline int f4_dstride(int cols) { return cols <= 32 ? 32 : cols <= 64 ? 64 : 128; }
+inline int f4_issuers(int cols) { return cols <= 64 ? 2 : 1; }
+struct F4Params {
+    uint16_t *y;          // [n][N] bf16 (swiglu: [n][N/2])
+    const float *gscale;  // device scalar g
+    uint8_t *xq;          // X codes: [K/256][f4_slot_bytes(cols)]
+    float *xs;            // [16][kF4Terms] the tokens' term scales
+    float *partials;      // [ctas][max_seg][128 rows][16] fp32 parts of split row blocks
+    unsigned *counters;   // [row_blocks] parts completed (zero between calls)
+    unsigned *err;        // device error word
+    int n, N, K, KC;      // KC = K / 256
+    int ctas, row_blocks, max_seg, stages, cols, swiglu, w_keep;
+    int inflight;         // weight stages requested and not yet landed, at most
+    int x_resident;       // 1: all unit columns' X codes stay in shared memory; 0: streamed with each stage
+};
+int f4_smem_bytes(int stages, int cols, bool x_resident, int KC);
+int f4_max_stages(int cols, int smem_limit, bool x_resident, int KC);   // 0: does not fit
+cudaError_t f4_set_smem_limit(int smem_optin);
+// X prep then GEMV, both with programmatic dependent launch.
+cudaError_t launch_fp4(const CUtensorMap &tw, const CUtensorMap &ts, const uint16_t *x, const F4Params &p, int smem,
+                       cudaStream_t stream);
 
 // Grouped read-once GEMV over routed experts (moe_gemv.cu).
 struct MoeParams {
