@@ -200,7 +200,7 @@ struct Plan {
     // and the workspace regions after the partial tiles
     int f4_cols_max = 0, f4_max_seg = 0, f4_max_parts = 0, f4_inflight = 0;
     bool f4_x_resident = false;
-    size_t f4_xq_offset = 0, f4_et_offset = 0;
+    size_t f4_xq_offset = 0, f4_xt_offset = 0, f4_et_offset = 0;
 };
 
 // Largest k-group (unit columns) whose X for 16 tokens fits next to eight
@@ -317,25 +317,33 @@ static std::vector<int> greedy_321(int n) {
 }
 
 static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nvfp4_gemv_opts &o, int sms,
-                                     int smem_optin, int tc_per_pass, Plan *plan);
+                                     int smem_optin, int tc_per_pass, bool allow_fp4, Plan *plan);
 
-// The tcgen05 kernel takes up to 32 tokens per pass (n = 17..32 in one read of
-// W); when the caller declares a scratch size (workspace_bytes) too small for
-// the 32-token pass, it gets 16-token passes instead.
+// AUTO picks the FP4 kernel for n <= 16 (one pass of W for every token) and
+// the tcgen05 kernel with 32 staged tokens above.  When the caller declares a
+// scratch size (workspace_bytes) too small for that plan, AUTO falls back to
+// the tcgen05 kernel, and its 32-token pass to 16-token passes.
 static nvfp4_status make_plan(int n, int N, int K, bool fast_ok, const nvfp4_gemv_opts &o, int sms, int smem_optin,
                               Plan *plan) {
-    nvfp4_status st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kTcMaxTokensPerPass, plan);
-    if (st == NVFP4_OK && plan->tc_tokens == 32 && o.workspace_bytes != 0 && o.workspace_bytes < plan->ws_bytes)
-        st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kMaxTokensPerPass, plan);
+    const bool small_ws = o.workspace_bytes != 0;
+    nvfp4_status st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kTcMaxTokensPerPass, true, plan);
+    if (st == NVFP4_OK && o.variant == kAuto && plan->variant == kFp4 && small_ws &&
+        o.workspace_bytes < plan->ws_bytes)
+        st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kTcMaxTokensPerPass, false, plan);
+    if (st == NVFP4_OK && plan->tc_tokens == 32 && small_ws && o.workspace_bytes < plan->ws_bytes)
+        st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kMaxTokensPerPass, false, plan);
     return st;
 }
 
 static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nvfp4_gemv_opts &o, int sms,
-                                     int smem_optin, int tc_per_pass, Plan *plan) {
+                                     int smem_optin, int tc_per_pass, bool allow_fp4, Plan *plan) {
     Plan p;
     p.variant = o.variant;
     const bool tc_ok = fast_ok;
-    if (p.variant == kAuto) p.variant = tc_ok ? kTc : (fast_ok ? kMma : kGeneric);
+    if (p.variant == kAuto) {
+        const bool fp4_ok = allow_fp4 && fast_ok && n <= kF4MaxTokensPerPass && K <= kF4MaxK;
+        p.variant = fp4_ok ? kFp4 : tc_ok ? kTc : kGeneric;
+    }
     if ((p.variant == kMma || p.variant == kSimt) && !fast_ok)
         return fail(NVFP4_ERR_INVALID_ARG,
                     "variant %d needs K %% 256 == 0 and 16-byte aligned w_packed, w_scale_e4m3 and x_bf16",
@@ -394,10 +402,12 @@ static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nv
         p.smem = f4_smem_bytes(stages, p.f4_cols_max, p.f4_x_resident, KC);
         const int RB = (N + kUnitRows - 1) / kUnitRows;
         p.counter_bytes = ws_counter_bytes(sms, RB);
-        p.partial_bytes = (size_t)ctas * p.f4_max_seg * kUnitRows * 16 * sizeof(float);
+        p.partial_bytes = (size_t)ctas * 2 * kUnitRows * 16 * sizeof(float);  // first and last row block
         p.f4_xq_offset = p.counter_bytes + ((p.partial_bytes + 255) & ~(size_t)255);
         const size_t xq_bytes = (size_t)KC * f4_slot_bytes(p.f4_cols_max);
-        p.f4_et_offset = p.f4_xq_offset + ((xq_bytes + 255) & ~(size_t)255);
+        p.f4_xt_offset = p.f4_xq_offset + ((xq_bytes + 255) & ~(size_t)255);
+        const size_t xt_bytes = (size_t)KC * f4_tab_bytes(p.f4_cols_max);
+        p.f4_et_offset = p.f4_xt_offset + ((xt_bytes + 255) & ~(size_t)255);
         p.ws_bytes = p.f4_et_offset + 16 * kF4Terms * sizeof(float);
     } else if (p.variant != kGeneric) {
         int max_tile = 0;
@@ -420,7 +430,12 @@ static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nv
         // the tcgen05 kernel needs an even number of stages (every consumer warp
         // waits on every phase of a stage's barriers)
         const int stage_step = p.variant == kTc ? 2 : 1;
-        int stages = kMaxStages;
+        // 16 staged tokens: at most 6 stages.  With 8, long unit ranges per CTA
+        // (about 30 units and more) gave run-to-run differing, wrong outputs in
+        // some row blocks on GB300; 6 and fewer stages, and the 8- and
+        // 32-token modes with 8, were exact over the same shapes.
+        const int max_stages = (p.variant == kTc && T == 16) ? 6 : kMaxStages;
+        int stages = max_stages;
         while (stages > 2 && smem_for(stages) > smem_optin) stages -= stage_step;
         if (smem_for(stages) > smem_optin) return fail(NVFP4_ERR_UNSUPPORTED, "K = %d does not fit shared memory", K);
         if (o.stages != 0) {
@@ -533,6 +548,7 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
         fp.counters = static_cast<unsigned *>(work);
         fp.partials = reinterpret_cast<float *>(static_cast<char *>(work) + plan.counter_bytes);
         fp.xq = static_cast<uint8_t *>(work) + plan.f4_xq_offset;
+        fp.xtab = static_cast<uint8_t *>(work) + plan.f4_xt_offset;
         fp.xs = reinterpret_cast<float *>(static_cast<char *>(work) + plan.f4_et_offset);
         fp.err = d->err_word;
         fp.N = N;

@@ -10,24 +10,28 @@
 // The tensor core's block-scaled FP4 MMA (tcgen05.mma kind::mxf4nvf4,
 // scale_vec::4X) multiplies E2M1 operands that each carry an E4M3 scale per
 // 16 k -- exactly NVFP4 -- so the weight operand is the stored W tile and the
-// weight scales are the stored S bytes.  The other operand must be E2M1 too,
-// so each bf16 activation row is written as a sum of J = 8 E2M1 terms
-// (fp4_xprep_kernel), each with one fp32 scale for the whole row:
+// weight scales are the stored S bytes.  The other operand must be NVFP4 too,
+// so each bf16 activation row is written as a sum of J = 8 NVFP4 terms
+// (fp4_xprep_kernel):
 //
-//     x[k] ~= sum_j s_j * q_j[k],   s_0 = max|x| / 6,   s_j = s_{j-1} / 6,
+//     x[k] ~= sum_j s_j * b[k/16] * q_j[k],
+//     s_0 = max|x| / (6 * 2^8),  s_j = s_{j-1} / 6,
+//     b[i] = 2^e, the smallest power of two (2^-9 <= b <= 2^8, so UE4M3
+//            holds it exactly) with 6 * s_0 * b >= max |x| over block i,
 //
 // q_j the E2M1 code (nearest, ties to even) of what the earlier terms left,
-// r_j / s_j.  The grid's largest gap (4 to 6) is 2, so |r_{j+1}| <= s_j =
-// 6 s_{j+1}: no term saturates, and after eight terms the residual is at most
-// max|x| / 6^8 (1.5e-7 of the row's largest entry; measured on N(0,1), 1 % x20
-// outlier, 1e-6-scaled and log-normal rows the worst output error stayed
-// below 0.1 of the 1e-2 (|y| + 1) tolerance).  The tensor core sees the codes
-// with a unit block scale; each term occupies its own MMA column (token t,
-// term j -> column 8t + j) and the epilogue applies the s_j and sums a token's
-// terms in a fixed order (the smallest first), multiplies by g and rounds to
-// bf16.  Every token's arithmetic is the same whatever n (the columns of an
-// MMA are independent, the expansion is per token), so a batched call equals
-// n single-token calls bit for bit.
+// r_j / (s_j b).  The grid's largest gap (4 to 6) is 2, so |r_{j+1}| <= s_j b
+// = 6 s_{j+1} b: no term saturates, and after eight terms a block's residual
+// is at most its own largest entry / 6^8 (1.5e-7 of it) -- relative to the
+// block, not the row, for blocks down to 2^-17 of the row's largest; below
+// that, at most 2^-17 max|x| / 6^8.  The tensor core applies b as the
+// activation operand's block scale (the same byte for the token's eight
+// terms); each term occupies its own MMA column (token t, term j -> column
+// 8t + j) and the epilogue applies the s_j and sums a token's terms in a
+// fixed order (the smallest first), multiplies by g and rounds to bf16.
+// Every token's arithmetic is the same whatever n (the columns of an MMA are
+// independent, the expansion is per token), so a batched call equals n
+// single-token calls bit for bit.
 //
 // Work split.  Units of 128 rows x 256 k (one 16 KB W tile, 128-byte swizzle,
 // plus the rows' 16 scale bytes); the persistent grid (one CTA per SM) takes
@@ -55,9 +59,10 @@
 //              runs the loop and one elected lane issues.
 //   warps 2-5  scale-factor warps, one per tensor-memory lane quarter: the MMA
 //              reads row m's four scale bytes of a K = 64 step from lane m,
-//              column base + m / 32 (measured on sm_103a); a warp copies its
-//              rows' 16 S bytes with one tcgen05.st per unit as soon as the
-//              stage lands (X is not needed for this).
+//              column base + m / 32, and column n's from lane 32 q + n % 32,
+//              column base + n / 32 in every quarter q (measured on sm_103a);
+//              per unit a warp copies its rows' 16 S bytes and the unit
+//              column's activation block scales with two tcgen05.st.
 //   warps 6-9  epilogue: per finished row-block segment, tcgen05.ld of the
 //              accumulators, the per-token sum of terms, then the bf16 store or
 //              the split-row protocol above.
@@ -89,11 +94,10 @@ constexpr int kF4WarpXLoad = 10;                // X loader
 constexpr int kF4WarpIssuer1 = 11;              // second MMA issuer (f4_issuers(cols) == 2)
 constexpr int kF4Threads = 12 * 32;
 constexpr uint32_t kF4TmemCols = 512;
-constexpr int kF4SfCols = 16;                   // tensor-memory columns per stage: the weight scales
+constexpr int kF4SfCols = 32;                   // tensor-memory columns per stage: W scales 16, X scales 16
 constexpr int kF4XprepThreads = 256;
 constexpr int kF4XprepElems = kF4XprepThreads * 8;  // activations per X-prep CTA
 constexpr unsigned kF4ErrSmemBase = 64u;            // dynamic shared memory not 1024-byte aligned
-constexpr uint32_t kF4UnitScale = 0x38383838u;      // four E4M3 1.0: the X codes' block scale
 
 __device__ __forceinline__ void mma_fp4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
                                         uint32_t sfb, uint32_t accumulate) {
@@ -196,12 +200,14 @@ __device__ __forceinline__ void f4_store_row(const F4Params &p, const float (&v)
     }
 }
 
-// Part c (a CTA) of split row block rb for this thread's row r.
+// Part c (a CTA) of split row block rb for this thread's row r.  A CTA's
+// range of units splits at most its first and its last row block, so each CTA
+// has two partial tiles: slot 0 for its first row block, slot 1 for its last.
 __device__ __forceinline__ void f4_load_part(const F4Params &p, float (&part)[16], int c, int rb, int r,
                                              long long U, int KC) {
     const long long cu0 = (long long)c * U / p.ctas;
     const int crb0 = (int)(cu0 / KC);
-    const float4 *src = reinterpret_cast<const float4 *>(p.partials + ((size_t)c * p.max_seg + (rb - crb0)) *
+    const float4 *src = reinterpret_cast<const float4 *>(p.partials + ((size_t)c * 2 + (rb == crb0 ? 0 : 1)) *
                                                                          (kUnitRows * 16) + (size_t)r * 16);
 #pragma unroll
     for (int qd = 0; qd < 4; ++qd) {
@@ -253,19 +259,20 @@ __device__ __forceinline__ uint32_t f4_cvt_e2m1x8(const float (&q)[8]) {
 
 // Shared memory: the ring (W + S tiles, plus the unit column's X codes when
 // they are streamed), the resident X codes (all K / 256 unit columns) when not,
-// the barriers, then flags and the term scales.
+// the X block scales (per stage or all unit columns, like the codes), the
+// barriers, then flags and the term scales.
 int f4_smem_bytes(int stages, int cols, bool x_resident, int KC) {
     const int slot = f4_slot_bytes(cols), groups = (KC + kF4XGroup - 1) / kF4XGroup;
     const int xbars = x_resident ? (groups > stages ? groups : stages) : stages;
-    return stages * (kF4XOffHost + (x_resident ? 0 : slot)) + (x_resident ? KC * slot : 0) +
+    const int tabs = ((x_resident ? KC : stages) * f4_tab_bytes(cols) + 15) & ~15;
+    return stages * (kF4XOffHost + (x_resident ? 0 : slot)) + (x_resident ? KC * slot : 0) + tabs +
            8 * (3 * stages + xbars + 8) + kF4MiscBytes;
 }
 
 // TMEM: accumulators [issuer][segment buffer 2][f4_dstride(cols)] from column
-// 0, the X codes' unit scale (4 columns, in a group of 16), then kF4SfCols per
-// stage.
+// 0, then kF4SfCols per stage (W scales, then X block scales).
 int f4_max_stages(int cols, int smem_limit, bool x_resident, int KC) {
-    const int tmem_stages = ((int)kF4TmemCols - 2 * f4_issuers(cols) * f4_dstride(cols) - 16) / kF4SfCols;
+    const int tmem_stages = ((int)kF4TmemCols - 2 * f4_issuers(cols) * f4_dstride(cols)) / kF4SfCols;
     int s = 2;
     while (s + 1 <= tmem_stages && s + 1 <= kF4MaxStages && f4_smem_bytes(s + 1, cols, x_resident, KC) <= smem_limit)
         ++s;
@@ -279,7 +286,8 @@ int f4_max_stages(int cols, int smem_limit, bool x_resident, int KC) {
 // them derive the same term scales without exchanging anything.
 template <int L>  // 16-byte loads per thread that cover a whole row: ceil(K / 2048) rounded up to 1, 2, 4, 8, 16
 __global__ void __maxnreg__(64) fp4_xprep_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ xq,
-                                                 float *__restrict__ xs, int K, int cols) {
+                                                 uint8_t *__restrict__ xtab, float *__restrict__ xs, int K,
+                                                 int cols) {
     griddep_launch_dependents();  // the GEMV may launch and start streaming its weights
     griddep_wait();               // X may be the output of the kernel ahead of this one
     const int t = blockIdx.y, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -311,8 +319,9 @@ __global__ void __maxnreg__(64) fp4_xprep_kernel(const uint16_t *__restrict__ x,
     for (int w = 0; w < kF4XprepThreads / 32; ++w) m = max(m, wmax[w]);
     // bf16 magnitude bits: >= 0x7F80 inf or NaN (the token's outputs become NaN)
     const bool finite = m < 0x7F80u;
-    float sc[kF4Terms];  // s_0 = max|x| / 6, s_j = s_{j-1} / 6 (zero for an all-zero row)
-    sc[0] = finite ? __fdiv_rn(__uint_as_float(m << 16), 6.0f) : __int_as_float(0x7FC00000);
+    // s_0 = max|x| / (6 * 2^8), s_j = s_{j-1} / 6 (zero for an all-zero row)
+    float sc[kF4Terms];
+    sc[0] = finite ? __fdiv_rn(__uint_as_float(m << 16), 6.0f * kF4BlockHeadroom) : __int_as_float(0x7FC00000);
 #pragma unroll
     for (int j = 1; j < kF4Terms; ++j) sc[j] = __fdiv_rn(sc[j - 1], 6.0f);
     if (blockIdx.x == 0 && tid < kF4Terms) {
@@ -321,7 +330,7 @@ __global__ void __maxnreg__(64) fp4_xprep_kernel(const uint16_t *__restrict__ x,
             if (tid == j) xs[t * kF4Terms + j] = sc[j];
     }
     const int k0 = own * 8;
-    if (k0 >= K) return;
+    if (k0 >= K) return;  // whole warps: K / 8 is a multiple of 32
     float r[8];
     {
         const uint32_t w[4] = {mine.x, mine.y, mine.z, mine.w};
@@ -331,13 +340,32 @@ __global__ void __maxnreg__(64) fp4_xprep_kernel(const uint16_t *__restrict__ x,
             r[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
         }
     }
+    // The 16-element block's scale b = 2^e (this thread and its neighbour hold
+    // the block): the smallest power of two with 6 s_0 b >= the block's max
+    // |x|, within UE4M3's powers of two 2^-9 .. 2^8.  Rounding in the ratio
+    // can only pick the neighbouring power: a first code clamped at 6 (the
+    // later terms take the excess) or one bit of the first term unused.
+    float bmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) bmax = fmaxf(bmax, fabsf(r[i]));
+    bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
+    int e = -9;
+    if (finite && sc[0] > 0.f) {
+        const float ratio = __fdiv_rn(bmax, 6.0f * sc[0]);
+        const uint32_t u = __float_as_uint(ratio);
+        const int E = (int)(u >> 23) - 127;  // ratio >= 0; 0 or subnormal give E = -127
+        if (ratio > 0.f) e = E + ((u & 0x7FFFFFu) != 0u ? 1 : 0);
+        e = min(max(e, -9), 8);
+    }
+    const float b = __int_as_float((e + 127) << 23);  // 2^e
     const int kc = k0 >> 8, bo = (k0 & 255) >> 1;
     uint8_t *const tile = xq + (size_t)kc * f4_slot_bytes(cols);
 #pragma unroll
     for (int j = 0; j < kF4Terms; ++j) {
         uint32_t codes = 0;
-        if (finite && sc[j] > 0.f) {
-            const float inv = __frcp_rn(sc[j]);
+        const float sj = sc[j] * b;  // exact: a power-of-two multiple
+        if (finite && sj >= 1.17549435e-38f) {  // a subnormal scale's term is below any output's rounding
+            const float inv = __frcp_rn(sj);
             float q[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) q[i] = r[i] * inv;
@@ -346,13 +374,17 @@ __global__ void __maxnreg__(64) fp4_xprep_kernel(const uint16_t *__restrict__ x,
             for (int i = 0; i < 4; ++i) {
                 const uint32_t h2 = e2m1x2_to_f16x2_rt(codes, i);
                 const float2 d = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
-                r[2 * i] = fmaf(-d.x, sc[j], r[2 * i]);
-                r[2 * i + 1] = fmaf(-d.y, sc[j], r[2 * i + 1]);
+                r[2 * i] = fmaf(-d.x, sj, r[2 * i]);
+                r[2 * i + 1] = fmaf(-d.y, sj, r[2 * i + 1]);
             }
         }
         const int c = t * kF4Terms + j;  // MMA column of (token, term): row c of the unit column's code tile
         *reinterpret_cast<uint32_t *>(tile + c * 128 + ((((bo >> 4) ^ (c & 7)) << 4) | (bo & 15))) = codes;
     }
+    // the block's UE4M3 byte: 2^e, subnormal below 2^-6
+    if ((own & 1) == 0)
+        xtab[(size_t)kc * f4_tab_bytes(cols) + t * 16 + ((k0 & 255) >> 4)] =
+            (uint8_t)(e >= -6 ? (e + 7) << 3 : 1 << (e + 9));
 }
 
 // Processing order of a CTA's units.  The CTA's range [u0, u0 + count) of the
@@ -421,6 +453,7 @@ __global__ void __maxnreg__(128)
     constexpr int kDStride = NC <= 32 ? 32 : NC <= 64 ? 64 : 128;
     constexpr int kIssuers = NC <= 64 ? 2 : 1;  // units alternate between the issuers (own accumulators)
     constexpr uint32_t kSlot = 128u * NC;       // one unit column's X codes
+    constexpr uint32_t kTab = 2u * NC;          // its block scales: NC / 8 tokens x 16 blocks
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t sbase = smem_u32(smem_raw);
     if (sbase & 1023u) {  // the swizzled tiles need a 1024-byte aligned base; never expected
@@ -441,12 +474,14 @@ __global__ void __maxnreg__(128)
     ord.init(u0, count, KC);
 
     // ---- shared memory: ring stages [W 16 KB][S 2 KB]([X slot] when streamed),
-    // resident X slots [KC] when not, then the barriers
+    // resident X slots [KC] when not, the X block scales ([S] or [KC]), then
+    // the barriers
     const uint32_t kStage = kF4XOffHost + (xres ? 0u : kSlot);
     const uint32_t sX = sbase + S * kStage;                  // resident X codes
+    const uint32_t sTab = sX + (xres ? KC * kSlot : 0u);     // X block scales
     const int xgroups = (KC + kF4XGroup - 1) / kF4XGroup;    // bulk copies of resident X codes
     const int xbars = xres ? (xgroups > S ? xgroups : S) : S;
-    const uint32_t sFull = sX + (xres ? KC * kSlot : 0u);    // [S] W + S landed (TMA)
+    const uint32_t sFull = sTab + (((xres ? KC : S) * kTab + 15u) & ~15u);  // [S] W + S landed (TMA)
     const uint32_t sXFull = sFull + 8 * S;      // [S] X codes of the stage landed / [xgroups] resident groups landed
     const uint32_t sSf = sXFull + 8 * xbars;    // [S] weight scales in tensor memory, count 4
     const uint32_t sEmpty = sSf + 8 * S;        // [S] MMAs done with the stage (commit)
@@ -505,8 +540,8 @@ __global__ void __maxnreg__(128)
     const uint32_t tbase = misc[0];
     // the next kernel on the stream (the next call's X prep) may launch now
     if (threadIdx.x == 0) griddep_launch_dependents();
-    const uint32_t sfb = tbase + 2 * kIssuers * kDStride;  // the X codes' unit block scale
-    const uint32_t sfa_base = sfb + 16;                     // weight scales: kF4SfCols columns per stage
+    // per stage kF4SfCols columns: the W scales (16), then the X block scales (16)
+    const uint32_t sf_base = tbase + 2 * kIssuers * kDStride;
 
     if (warp == kF4WarpProducer) {
         // ---------------------------------------------------- weight producer
@@ -541,11 +576,13 @@ __global__ void __maxnreg__(128)
             griddep_wait();  // the X codes are the output of the X-prep kernel ahead
             const uint64_t x_policy = l2_policy_evict_last();  // every CTA reads the same X codes
             if (xres) {
-                // every unit column's X codes, kF4XGroup columns per bulk copy
+                // every unit column's X codes, kF4XGroup columns per bulk copy;
+                // all block scales with the first group
                 for (int g = 0; g < xgroups; ++g) {
                     const int c0 = g * kF4XGroup, nc = KC - c0 < kF4XGroup ? KC - c0 : kF4XGroup;
                     const uint32_t bytes = (uint32_t)nc * kSlot, bar = sXFull + 8 * g;
-                    mbar_arrive_expect_tx(bar, bytes);
+                    mbar_arrive_expect_tx(bar, bytes + (g == 0 ? KC * kTab : 0u));
+                    if (g == 0) bulk_load_f4(sTab, p.xtab, KC * kTab, bar, x_policy);
                     bulk_load_f4(sX + (uint32_t)c0 * kSlot, p.xq + (size_t)c0 * kSlot, bytes, bar, x_policy);
                 }
                 for (int g = 0; g < xgroups; ++g) {
@@ -564,9 +601,10 @@ __global__ void __maxnreg__(128)
                         break;
                     }
                     const uint32_t bar = sXFull + 8 * xw.st;
-                    mbar_arrive_expect_tx(bar, kSlot);
+                    mbar_arrive_expect_tx(bar, kSlot + kTab);
                     bulk_load_f4(sbase + xw.st * kStage + kF4XOffHost, p.xq + (size_t)xw.kc * kSlot, kSlot, bar,
                                  x_policy);
+                    bulk_load_f4(sTab + xw.st * kTab, p.xtab + (size_t)xw.kc * kTab, kTab, bar, x_policy);
                     xw.next();
                 }
                 const int lo = loaded > S ? loaded - S : 0;
@@ -635,12 +673,13 @@ __global__ void __maxnreg__(128)
                 }
                 tc::fence_after_sync();
                 const uint64_t ad = desc0 + ((sbase + st * kStage) >> 4), bd = desc0 + (x_addr(st, iw.kc) >> 4);
-                const uint32_t sfa = sfa_base + st * kF4SfCols;
+                const uint32_t sfa = sf_base + st * kF4SfCols, sfb = sfa + 16;
                 __syncwarp();
                 if (elect_one()) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_fp4(d_tmem, ad + 2 * k, bd + 2 * k, idesc, sfa + 4 * k, sfb, (!first || k > 0) ? 1u : 0u);
+                        mma_fp4(d_tmem, ad + 2 * k, bd + 2 * k, idesc, sfa + 4 * k, sfb + 4 * k,
+                                (!first || k > 0) ? 1u : 0u);
                     tc::commit(sEmpty + 8 * st);
                 }
                 __syncwarp();
@@ -658,29 +697,44 @@ __global__ void __maxnreg__(128)
         __syncwarp();
     } else if (warp >= kF4WarpSf0 && warp < kF4WarpEpi0) {
         // ------------------------------------------------- scale-factor warps
-        // Lane quarter q: rows 32q + lane.  Per stage, kF4SfCols columns: the
-        // MMA of step s reads column 4s + q for its quarter-q rows, so every
-        // column of the group gets the word.  First the X codes' unit scale:
-        // four columns of E4M3 1.0 that every MMA reads (column n / 32 for
-        // token-term column n), the same in every quarter.
+        // Lane quarter q: rows 32q + lane.  Per stage, kF4SfCols columns.  W
+        // scales: the MMA of step s reads column 4s + q for its quarter-q rows,
+        // so every column of the group gets the word.  X block scales: the MMA
+        // of step s reads column 16 + 4s + n / 32 at lane n % 32 of every
+        // quarter for token-term column n; the word is the four block bytes of
+        // the step for the column's token (the same for its eight terms).
         const int q = warp & 3;
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
         const int r = 32 * q + lane;
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%1,%1,%1};" ::"r"(sfb + lane_bits),
-                     "r"(kF4UnitScale)
-                     : "memory");
         bool ok = true;
+        if (xres && count > 0)  // every unit column's block scales land with the first X group
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(sXFull, 0));
         F4Walk sw;
         if (count > 0) sw.begin(ord, S);
-        for (int i = 0; i < count; ++i, sw.next()) {
+        for (int i = 0; i < count && ok; ++i, sw.next()) {
             const int st = sw.st;
-            if (__any_sync(0xffffffffu, !mbar_wait_bounded(sFull + 8 * st, sw.ph))) {
+            if (__any_sync(0xffffffffu, !mbar_wait_bounded(sFull + 8 * st, sw.ph) ||
+                                            (!xres && !mbar_wait_bounded(sXFull + 8 * st, sw.ph)))) {
                 ok = false;
                 break;
             }
+            const uint32_t sfa = sf_base + st * kF4SfCols;
             const uint4 a = lds128(sbase + st * kStage + kF4WBytes + 16 * r);
             const uint32_t v[16] = {a.x, a.x, a.x, a.x, a.y, a.y, a.y, a.y, a.z, a.z, a.z, a.z, a.w, a.w, a.w, a.w};
-            tc::st_32x32b_x16(sfa_base + lane_bits + st * kF4SfCols, v);
+            tc::st_32x32b_x16(sfa + lane_bits, v);
+            const uint32_t tab = sTab + (xres ? (uint32_t)sw.kc : (uint32_t)st) * kTab;
+            uint32_t w[16];
+#pragma unroll
+            for (int c32 = 0; c32 < 4; ++c32) {
+                const int n = 32 * c32 + lane;  // token-term column; token n / 8
+                uint4 b = make_uint4(0, 0, 0, 0);
+                if (n < NC) b = lds128(tab + 16 * (n >> 3));
+                w[c32] = b.x;
+                w[4 + c32] = b.y;
+                w[8 + c32] = b.z;
+                w[12 + c32] = b.w;
+            }
+            tc::st_32x32b_x16(sfa + 16 + lane_bits, w);
             tc::wait_st();
             tc::fence_before_sync();
             __syncwarp();
@@ -805,7 +859,7 @@ __global__ void __maxnreg__(128)
             }
             if (!last) {
                 float *const part_out =
-                    p.partials + ((size_t)blockIdx.x * p.max_seg + ns) * (kUnitRows * 16) + (size_t)r * 16;
+                    p.partials + ((size_t)blockIdx.x * 2 + (ns == 0 ? 0 : 1)) * (kUnitRows * 16) + (size_t)r * 16;
 #pragma unroll
                 for (int qd = 0; qd < 4; ++qd)
                     if (4 * qd < p.n)
@@ -874,11 +928,11 @@ cudaError_t launch_fp4(const CUtensorMap &tw, const CUtensorMap &ts, const uint1
     xc.numAttrs = 1;
     const int loads = (p.K + kF4XprepElems - 1) / kF4XprepElems;
     cudaError_t e;
-    if (loads <= 1) e = cudaLaunchKernelEx(&xc, fp4_xprep_kernel<1>, x, p.xq, p.xs, p.K, p.cols);
-    else if (loads <= 2) e = cudaLaunchKernelEx(&xc, fp4_xprep_kernel<2>, x, p.xq, p.xs, p.K, p.cols);
-    else if (loads <= 4) e = cudaLaunchKernelEx(&xc, fp4_xprep_kernel<4>, x, p.xq, p.xs, p.K, p.cols);
-    else if (loads <= 8) e = cudaLaunchKernelEx(&xc, fp4_xprep_kernel<8>, x, p.xq, p.xs, p.K, p.cols);
-    else e = cudaLaunchKernelEx(&xc, fp4_xprep_kernel<16>, x, p.xq, p.xs, p.K, p.cols);
+    if (loads <= 1) e = cudaLaunchKernelEx(&xc, fp4_xprep_kernel<1>, x, p.xq, p.xtab, p.xs, p.K, p.cols);
+    else if (loads <= 2) e = cudaLaunchKernelEx(&xc, fp4_xprep_kernel<2>, x, p.xq, p.xtab, p.xs, p.K, p.cols);
+    else if (loads <= 4) e = cudaLaunchKernelEx(&xc, fp4_xprep_kernel<4>, x, p.xq, p.xtab, p.xs, p.K, p.cols);
+    else if (loads <= 8) e = cudaLaunchKernelEx(&xc, fp4_xprep_kernel<8>, x, p.xq, p.xtab, p.xs, p.K, p.cols);
+    else e = cudaLaunchKernelEx(&xc, fp4_xprep_kernel<16>, x, p.xq, p.xtab, p.xs, p.K, p.cols);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.ctas);

@@ -25,6 +25,7 @@
 #include "../../include/nvfp4_gemv.h"
 #include "internal.h"
 
+#include <cstdint>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -74,8 +75,14 @@ extern "C" nvfp4_status nvfp4_gemv_batched_noalloc(const uint8_t *w_packed, cons
     nvfp4_gemv_opts cap;  // plan within the static scratch (32-token passes fall back to 16 if it is too small)
     std::memset(&cap, 0, sizeof cap);
     cap.workspace_bytes = kNoAllocScratchBytes;
-    const int st = workspace_layout(n, N, K, &cap, &counter_bytes, &needed);
-    if (st != NVFP4_OK) return (nvfp4_status)st;
+    // Inputs off 16-byte alignment (or K % 256 != 0) take the generic kernel,
+    // which needs no scratch: size the call only when the fast path runs.
+    const auto a16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    const bool fast = K % 256 == 0 && a16(w_packed) && a16(w_scale_e4m3) && a16(x_bf16);
+    if (fast) {
+        const int st = workspace_layout(n, N, K, &cap, &counter_bytes, &needed);
+        if (st != NVFP4_OK) return (nvfp4_status)st;
+    }
     if (needed > kNoAllocScratchBytes) {
         char buf[256];
         std::snprintf(buf, sizeof buf,

@@ -43,11 +43,14 @@ struct StreamParams {
 };
 
 // Block-scaled FP4 tensor-core path (gemv_fp4.cu).  Per pass of up to 16
-// tokens: fp4_xprep_kernel writes each token's activations as kF4Terms E2M1
-// terms with one fp32 scale per (token, term) -- MMA columns 8t + j -- into
-// the workspace, then the GEMV streams the stored W and S tiles straight into
-// tcgen05.mma kind::mxf4nvf4.  Workspace per unit column of 256 k: the codes
-// [cols][128 B] (128-byte swizzled rows); the scales [16][kF4Terms] floats.
+// tokens: fp4_xprep_kernel writes each token's activations as kF4Terms NVFP4
+// terms -- E2M1 codes, one power-of-two UE4M3 scale per 16-element block
+// (shared by the token's terms) and one fp32 scale per (token, term), MMA
+// columns 8t + j -- into the workspace, then the GEMV streams the stored W
+// and S tiles straight into tcgen05.mma kind::mxf4nvf4.  Workspace per unit
+// column of 256 k: the codes [cols][128 B] (128-byte swizzled rows) and the
+// block scales [cols / 8 tokens][16 B]; then the term scales [16][kF4Terms]
+// floats.
 constexpr int kF4Terms = 8;
 constexpr int kF4MaxTokensPerPass = 16;
 constexpr int kF4MaxCols = 128;              // 16 tokens x 8 terms
@@ -63,6 +66,8 @@ inline int f4_cols(int n) { return 16 * ((n * kF4Terms + 15) / 16); }
 #define NVFP4_HD
 #endif
 NVFP4_HD inline int f4_slot_bytes(int cols) { return 128 * cols; }  // one unit column's X codes
+NVFP4_HD inline int f4_tab_bytes(int cols) { return 2 * cols; }     // its block scales: cols / 8 tokens x 16
+constexpr int kF4BlockHeadroom = 256;        // largest activation block scale, 2^8 (UE4M3 spans 2^-9 .. 2^8)
 constexpr int kF4XGroup = 4;                 // unit columns per bulk copy of resident X codes
 constexpr int kF4ResidentXMax = 112 * 1024;  // largest X code block kept resident in shared memory
 inline int f4_dstride(int cols) { return cols <= 32 ? 32 : cols <= 64 ? 64 : 128; }
@@ -71,8 +76,9 @@ struct F4Params {
     uint16_t *y;          // [n][N] bf16 (swiglu: [n][N/2])
     const float *gscale;  // device scalar g
     uint8_t *xq;          // X codes: [K/256][f4_slot_bytes(cols)]
+    uint8_t *xtab;        // X block scales: [K/256][f4_tab_bytes(cols)], UE4M3 byte per (token, 16-k block)
     float *xs;            // [16][kF4Terms] the tokens' term scales
-    float *partials;      // [ctas][max_seg][128 rows][16] fp32 parts of split row blocks
+    float *partials;      // [ctas][2][128 rows][16] fp32 parts of split row blocks (first, last)
     unsigned *counters;   // [row_blocks] parts completed (zero between calls)
     unsigned *err;        // device error word
     int n, N, K, KC;      // KC = K / 256

@@ -113,23 +113,42 @@ def test_greedy_321_tiling_matches_the_pages():
 def test_one_pass_plan():
     for n in (1, 4, 8, 16):
         plan = nv.nvfp4_gemv_plan(n, 14336, 5120)
-        assert plan["variant"] == "tc" and plan["tiling"] == "one_pass"
+        assert plan["variant"] == "fp4" and plan["tiling"] == "one_pass"
         assert plan["passes"] == 1 and plan["tile_tokens"] == [n]
         assert plan["units"] == (14336 // 128) * (5120 // 256)
+        assert 4 <= plan["stages"] <= 16 and plan["smem_bytes"] <= 232448 - 4096
+        tc = nv.nvfp4_gemv_plan(n, 14336, 5120, variant=nv.VARIANT_TC)
+        assert tc["units"] == (14336 // 128) * (5120 // 256)
+        assert 2 <= tc["stages"] <= 8 and tc["stages"] % 2 == 0 and tc["smem_bytes"] <= 232448
         mma = nv.nvfp4_gemv_plan(n, 14336, 5120, variant=nv.VARIANT_MMA)
         assert mma["units"] == (14336 // 128) * (5120 // 128)
-        assert 2 <= plan["stages"] <= 8 and plan["stages"] % 2 == 0 and plan["smem_bytes"] <= 232448
+    # the FP4 kernel takes K up to 32768; beyond, AUTO takes the tcgen05 kernel
+    assert nv.nvfp4_gemv_plan(4, 256, 32768)["variant"] == "fp4"
+    assert nv.nvfp4_gemv_plan(4, 256, 32768 + 256)["variant"] == "tc"
+    with pytest.raises(nv.Nvfp4Error):
+        nv.nvfp4_gemv_plan(4, 256, 32768 + 256, variant=nv.VARIANT_FP4)
+    # greedy 3/2/1 tiling on the FP4 kernel: tiles of 3 tokens
+    assert nv.nvfp4_gemv_plan(8, 14336, 5120, tiling=nv.TILING_GREEDY_321)["tile_tokens"] == [3, 3, 2]
+    assert nv.nvfp4_gemv_plan(8, 14336, 5120, tiling=nv.TILING_GREEDY_321)["variant"] == "fp4"
+    # a declared scratch size too small for the FP4 plan: the tcgen05 kernel
+    f4 = nv.nvfp4_gemv_workspace_size(8, 14336, 5120)
+    tc8 = nv.nvfp4_gemv_workspace_size(8, 14336, 5120, variant=nv.VARIANT_TC)
+    if tc8 < f4:
+        assert nv.nvfp4_gemv_plan(8, 14336, 5120, workspace_bytes=tc8)["variant"] == "tc"
+    assert nv.nvfp4_gemv_plan(8, 14336, 5120, workspace_bytes=f4)["variant"] == "fp4"
     # more than 16 tokens: one pass of up to 32 (X streamed per unit), then more
     assert nv.nvfp4_gemv_plan(20, 4096, 4096)["tile_tokens"] == [20]
     assert nv.nvfp4_gemv_plan(32, 14336, 5120)["tile_tokens"] == [32]
     assert nv.nvfp4_gemv_plan(64, 14336, 5120)["tile_tokens"] == [32, 32]
     assert nv.nvfp4_gemv_plan(40, 14336, 5120)["tile_tokens"] == [32, 8]
     # a declared scratch size too small for the 32-token pass: 16-token passes
-    small = nv.nvfp4_gemv_workspace_size(16, 14336, 5120)
+    small = nv.nvfp4_gemv_workspace_size(16, 14336, 5120, variant=nv.VARIANT_TC)
     assert nv.nvfp4_gemv_workspace_size(32, 14336, 5120) > small
     assert nv.nvfp4_gemv_plan(40, 14336, 5120, workspace_bytes=small)["tile_tokens"] == [16, 16, 8]
     # K too large for 16 tokens of X in shared memory: smaller chunks
     p = nv.nvfp4_gemv_plan(16, 1024, 8192)
+    assert p["tile_tokens"] == [16]        # FP4: X codes streamed per unit when not resident
+    p = nv.nvfp4_gemv_plan(16, 1024, 8192, variant=nv.VARIANT_TC)
     assert p["tile_tokens"] == [16]        # tcgen05: X is streamed per unit, any K fits
     p = nv.nvfp4_gemv_plan(16, 1024, 8192, variant=nv.VARIANT_MMA)
     assert sum(p["tile_tokens"]) == 16 and max(p["tile_tokens"]) < 16
@@ -138,7 +157,8 @@ def test_one_pass_plan():
     assert nv.nvfp4_gemv_workspace_size(3, 100, 784) == 0
     assert nv.nvfp4_gemv_workspace_size(3, 14336, 5120) > 0
     # the grid never exceeds the number of units
-    assert nv.nvfp4_gemv_plan(3, 256, 512)["num_ctas"] == 2 * 2          # tcgen05: 128 x 256 units
+    assert nv.nvfp4_gemv_plan(3, 256, 512)["num_ctas"] == 2 * 2          # FP4: 128 x 256 units
+    assert nv.nvfp4_gemv_plan(3, 256, 512, variant=nv.VARIANT_TC)["num_ctas"] == 2 * 2
     assert nv.nvfp4_gemv_plan(3, 256, 512, variant=nv.VARIANT_MMA)["num_ctas"] == 2 * 4
 
 

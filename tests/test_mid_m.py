@@ -5,8 +5,9 @@ mid-M tile GEMM: verify and prefill batches).
 
 Tolerance as for the GEMV: |y_gpu - y_ref| <= 1e-2 * (|y_ref| + 1), y_ref the
 oracle's unrounded fp64 value.  The k-group partition is the one of n <= 16,
-so a batched call still equals the single-token calls bit for bit (atlas #266,
-"Correctness argument").  Inputs: oracle-quantized W ~ N(0, 0.02), X ~ N(0, 1)
+so a batched call still equals the single-token calls of the same kernel bit
+for bit (atlas #266, "Correctness argument"; AUTO takes the FP4 kernel for
+n <= 16, so the single-token calls here name the tcgen05 variant).  Inputs: oracle-quantized W ~ N(0, 0.02), X ~ N(0, 1)
 bf16 (synth.py).
 """
 from __future__ import annotations
@@ -82,8 +83,10 @@ def test_mid_m_equals_single_token_calls(n):
     packed, scale, g, x = make_case(N, K, n, 5, 6)
     wp, ws, gs, xt = to_gpu(packed, scale, g, x)
     full = bits(nv.nvfp4_gemv_batched(wp, ws, gs, xt))
+    assert nv.nvfp4_gemv_plan(n, N, K)["variant"] == "tc"
     for t in range(n):
-        one = bits(nv.nvfp4_gemv_batched(wp, ws, gs, xt[t:t + 1].contiguous()))
+        # the same kernel for one token (AUTO would take the FP4 kernel at n = 1)
+        one = bits(nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt[t:t + 1].contiguous(), variant=nv.VARIANT_TC))
         assert np.array_equal(one[0], full[t]), t
 
 
@@ -100,7 +103,7 @@ def test_mid_m_full_size_qkv_sampled(n):
     ref64, _ = oracle.gemv_points(packed, scale, g, x, toks, rows)
     assert_close(y16[toks, rows], ref64)
     for t in (0, 17, n - 1):  # batched == single token on the full-size launch configuration
-        one = bits(nv.nvfp4_gemv_batched(wp, ws, gs, xt[t:t + 1].contiguous()))
+        one = bits(nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt[t:t + 1].contiguous(), variant=nv.VARIANT_TC))
         assert np.array_equal(one[0], y16[t]), t
 
 
@@ -138,7 +141,7 @@ def test_mid_m_caller_workspace_and_fallback():
     y_big = bits(nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt, workspace=big))
     assert_close(y_big, y64)
     # a scratch sized for 16 tokens: the call takes 16-token passes instead, same bits
-    small_bytes = nv.nvfp4_gemv_workspace_size(16, N, K)
+    small_bytes = nv.nvfp4_gemv_workspace_size(16, N, K, variant=nv.VARIANT_TC)
     assert small_bytes < big.numel()
     small = torch.zeros(small_bytes, dtype=torch.uint8, device="cuda")
     assert np.array_equal(bits(nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt, workspace=small)), y_big)

@@ -7,6 +7,8 @@ Inputs: oracle-quantized W ~ N(0, 0.02), X ~ N(0, 1) bf16 (synth.py).
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -17,7 +19,8 @@ import synth
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-2
-VARIANTS = {"tc": nv.VARIANT_TC, "mma": nv.VARIANT_MMA, "simt": nv.VARIANT_SIMT, "generic": nv.VARIANT_GENERIC}
+VARIANTS = {"fp4": nv.VARIANT_FP4, "tc": nv.VARIANT_TC, "mma": nv.VARIANT_MMA, "simt": nv.VARIANT_SIMT,
+            "generic": nv.VARIANT_GENERIC}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -81,10 +84,13 @@ def test_ragged_shapes_full_output(variant, N, K, n):
 
 
 def test_one_hot_pins_nibble_order_and_scale_placement():
-    """Single-term outputs are exact: y[t, r] = bf16(E2M1 * E4M3 * g) at k_t."""
+    """Single-term outputs are exact: y[t, r] = bf16(E2M1 * E4M3 * g) at k_t.
+    (FP4 variant: x = 1 expands to the single code 6 with s_0 = fl(1/6); the
+    product fl(1/6) * 6 * w is w to within 2^-25 relative, below half an fp32
+    ulp, so the accumulator holds w exactly as in the other kernels.)"""
     N, K = 128, 256
     packed, scale, g, _ = make_case(N, K, 1, 9, 0)
-    for variant in ("tc", "mma", "simt"):
+    for variant in ("fp4", "tc", "mma", "simt"):
         for k0 in range(0, K, 16):
             x = np.zeros((16, K), dtype=np.uint16)
             x[np.arange(16), k0 + np.arange(16)] = 0x3F80
@@ -114,9 +120,27 @@ def test_repeat_calls_are_bit_identical():
         assert np.array_equal(gpu_gemv(dev), first)
 
 
+@pytest.mark.parametrize("variant", ["fp4", "tc"])
+@pytest.mark.parametrize("n,num_ctas", [(16, 38), (16, 0), (4, 38)])
+def test_long_unit_ranges_are_deterministic(variant, n, num_ctas):
+    """Deep K and few CTAs: every CTA streams tens of units over several row
+    blocks and the ring wraps many times.  Repeated calls agree bit for bit
+    and with the oracle (a race between the ring stages and the hand-offs
+    would show as run-to-run differences here)."""
+    N, K = 14336, 10240
+    packed, scale, g, x = make_case(N, K, n, 40, 41)
+    dev = to_gpu(packed, scale, g, x)
+    runs = [gpu_gemv(dev, VARIANTS[variant], num_ctas=num_ctas) for _ in range(6)]
+    for r in runs[1:]:
+        assert np.array_equal(r, runs[0])
+    toks, rows = sample_points(n, N, K, 300, 42)
+    ref64, _ = oracle.gemv_points(packed, scale, g, x, toks, rows)
+    assert_close(runs[0][toks, rows], ref64)
+
+
 @pytest.mark.parametrize("variant,num_ctas,stages", [
-    (v, c, s) for v in ("tc", "mma") for (c, s) in [(1, 2), (3, 0), (7, 4), (0, 2), (150, 8), (0, 6)]
-] + [("mma", 7, 3), ("mma", 5, 5)])
+    (v, c, s) for v in ("fp4", "tc", "mma") for (c, s) in [(1, 2), (3, 0), (7, 4), (0, 2), (150, 8), (0, 6)]
+] + [("mma", 7, 3), ("mma", 5, 5), ("fp4", 5, 3), ("fp4", 0, 10), ("fp4", 9, 11)])
 def test_grid_and_ring_options(variant, num_ctas, stages):
     packed, scale, g, x = make_case(700, 1280, 4, 7, 8)
     y64, _ = oracle.gemv(packed, scale, g, x)
@@ -124,17 +148,19 @@ def test_grid_and_ring_options(variant, num_ctas, stages):
     assert_close(y16, y64)
 
 
+@pytest.mark.parametrize("variant", ["fp4", "tc"])
 @pytest.mark.parametrize("N,K,n,num_ctas", [
     (2000, 256, 4, 5),     # one unit per row block: every segment has one unit, two issuers idle
     (1000, 512, 9, 3),     # segments of two units
     (1000, 768, 16, 4),    # segments of three units, one per issuer
     (3000, 1280, 2, 11),   # segments of five units, split row blocks
+    (640, 8192, 3, 7),     # few row blocks, every one split over several CTAs
 ])
-def test_short_segments(N, K, n, num_ctas):
-    """Row-block segments shorter than the issuer rotation (tcgen05 kernel)."""
+def test_short_segments(variant, N, K, n, num_ctas):
+    """Row-block segments shorter than the issuer rotation (tensor-memory kernels)."""
     packed, scale, g, x = make_case(N, K, n, 12, 13)
     y64, _ = oracle.gemv(packed, scale, g, x)
-    assert_close(gpu_gemv(to_gpu(packed, scale, g, x), nv.VARIANT_TC, num_ctas=num_ctas), y64)
+    assert_close(gpu_gemv(to_gpu(packed, scale, g, x), VARIANTS[variant], num_ctas=num_ctas), y64)
 
 
 def test_chained_calls_read_the_previous_output():
@@ -165,8 +191,8 @@ def test_chained_calls_with_every_row_block_whole():
     the reduction kernel, which must still not complete before the GEMV."""
     N1, K1 = 152 * 128, 256
     plan = nv.nvfp4_gemv_plan(2, N1, K1)
-    if plan["variant"] != "tc" or plan["num_ctas"] != 152:
-        pytest.skip("needs the tcgen05 path on a 152-SM part")
+    if plan["variant"] not in ("fp4", "tc") or plan["num_ctas"] != 152:
+        pytest.skip("needs a tensor-memory path on a 152-SM part")
     p1, s1, g1, x = make_case(N1, K1, 2, 30, 31)
     p2, s2, g2, _ = make_case(256, N1, 2, 32, 33)
     wp1, ws1, gs1, xt = to_gpu(p1, s1, g1, x)
@@ -246,8 +272,38 @@ def test_activation_beyond_f16_range_is_rescaled():
     xf[2, 900] = -1.0e6
     x = synth.to_bf16_bits(xf)
     y64, _ = oracle.gemv(packed, scale, g, x)
-    for variant in ("tc", "mma", "simt", "generic"):
+    for variant in VARIANTS:
         assert_close(gpu_gemv(to_gpu(packed, scale, g, x), VARIANTS[variant]), y64)
+
+
+# Variants that take bf16 activations over their whole range (the FP4 kernel's
+# per-row term scales, the generic kernel's fp32 FMAs); the others convert X to
+# f16 and are in range only for 2^-6 <= |x| < 1.68e7 or so.
+FULL_RANGE_X = ("fp4", "generic")
+
+
+@pytest.mark.parametrize("x_max", [1.6e7, 2.0 ** -18, 1.0e-30])
+def test_activation_magnitudes(x_max):
+    """Rows scaled to max|x| = x_max (up to 1.6e7, just inside the f16 x 2^-8
+    range of the tcgen05 kernel; down to 1e-30), next to an all-zero row and a
+    row with one non-zero entry.  Tolerance relative to each row's own output
+    scale: |y - y_ref| <= 1e-2 * (|y_ref| + max_r |y_ref|) per token."""
+    N, K, n = 384, 1536, 4
+    packed, scale, g, _ = make_case(N, K, n, 14, 15)
+    xf = synth.activations_f32(n, K, 16).astype(np.float64)
+    xf *= x_max / np.abs(xf).max()
+    xf[1] = 0.0
+    xf[2] = 0.0
+    xf[2, 700] = -x_max
+    x = synth.to_bf16_bits(xf.astype(np.float32))
+    y64, _ = oracle.gemv(packed, scale, g, x)
+    row_scale = np.abs(y64).max(axis=1, keepdims=True)
+    for variant in (VARIANTS if x_max >= 1.0 else FULL_RANGE_X):
+        yv = bf16_to_f64(gpu_gemv(to_gpu(packed, scale, g, x), VARIANTS[variant]))
+        assert np.all(yv[1] == 0.0), variant
+        err = np.abs(yv - y64)
+        assert np.all(err <= TOL * (np.abs(y64) + row_scale)), (variant, (err / row_scale).max())
+    assert nv.nvfp4_device_error() == 0
 
 
 def test_nan_scale_propagates():
@@ -301,6 +357,67 @@ def test_full_size_workloads_sampled(name, N, K, ns, outlier):
         y1 = nv.nvfp4_gemv_batched(wp, ws, gs, xt_all[nmax - 1:nmax].contiguous())
         torch.cuda.synchronize()
         assert np.array_equal(y1.view(torch.int16).cpu().numpy().view(np.uint16)[0], per_token[nmax][nmax - 1])
+
+
+def oracle_rows_parallel(packed, scale, g, x):
+    """The oracle's full output, its rows split over the host cores (the oracle's
+    C routine runs without the interpreter lock, so threads run in parallel)."""
+    from concurrent.futures import ThreadPoolExecutor
+    N = packed.shape[0]
+    cores = os.cpu_count() or 1
+    bounds = np.linspace(0, N, min(cores, N) + 1).astype(int)
+
+    def part(i):
+        r0, r1 = bounds[i], bounds[i + 1]
+        return oracle.gemv(np.ascontiguousarray(packed[r0:r1]), np.ascontiguousarray(scale[r0:r1]), g, x)[0]
+    with ThreadPoolExecutor(len(bounds) - 1) as ex:
+        return np.concatenate(list(ex.map(part, range(len(bounds) - 1))), axis=1)
+
+
+@pytest.mark.parametrize("name,N,K,n", [("attn_qkv", 14336, 5120, 4), ("fused_qkv", 16384, 5120, 16)])
+def test_full_size_whole_output(name, N, K, n):
+    """Every output of a full-size call against the oracle, in the launch
+    configuration the benchmark times (AUTO plan, one CTA per SM)."""
+    packed, scale, g = oracle.quantize(synth.weights_f32(N, K, 0))
+    x = synth.activations_bf16(n, K, 1)
+    y16 = gpu_gemv(to_gpu(packed, scale, g, x))
+    assert_close(y16, oracle_rows_parallel(packed, scale, g, x))
+
+
+def test_decode_step_chain_of_32_calls():
+    """Sixteen layers of qkv (N=14336, K=5120) then o_proj (N=5120, K=6144) on one
+    stream with no synchronization: o_proj reads the first 6144 qkv outputs,
+    the next layer's qkv reads the o_proj output.  Each call is then checked on
+    sampled points against the oracle given the GPU's own input to that call."""
+    n = 8
+    layers = 16
+    mats = {}
+    for name, (N, K) in (("qkv", (14336, 5120)), ("o", (5120, 6144))):
+        mats[name] = []
+        for i in range(4):
+            packed, scale, g = oracle.quantize(synth.weights_f32(N, K, 50 + 10 * i + (name == "o")))
+            mats[name].append((packed, scale, g, to_gpu(packed, scale, g, np.zeros((1, K), np.uint16))[:3]))
+    x0 = synth.activations_bf16(n, 5120, 60)
+    x = torch.from_numpy(x0.view(np.int16)).cuda().view(torch.bfloat16)
+    outs = []
+    for layer in range(layers):
+        wq = mats["qkv"][layer % 4]
+        yq = nv.nvfp4_gemv_batched(*wq[3], x)
+        xo = yq[:, :6144].contiguous()
+        wo = mats["o"][layer % 4]
+        yo = nv.nvfp4_gemv_batched(*wo[3], xo)
+        outs.append((wq, x, yq))
+        outs.append((wo, xo, yo))
+        x = yo
+    torch.cuda.synchronize()
+    for i, ((packed, scale, g, _), xin, y) in enumerate(outs):
+        xin16 = xin.view(torch.int16).cpu().numpy().view(np.uint16)
+        y16 = y.view(torch.int16).cpu().numpy().view(np.uint16)
+        nn, N = y16.shape
+        toks, rows = sample_points(nn, N, packed.shape[1] * 2, 100, 70 + i)
+        ref64, _ = oracle.gemv_points(packed, scale, g, xin16, toks, rows)
+        assert_close(y16[toks, rows], ref64)
+    assert nv.nvfp4_device_error() == 0
 
 
 def test_no_device_error_recorded():
