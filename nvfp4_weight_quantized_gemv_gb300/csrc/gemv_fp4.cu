@@ -170,6 +170,26 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
     return v;
 }
 
+// Count one published part: release (the CTA's partial-tile stores, ordered
+// before by the named barrier) and acquire (the other parts, for the CTA that
+// adds the last one) in one atomic.
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned *p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Non-blocking check of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, unsigned parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // One row's outputs for all n tokens (v[t] = token t's sum of terms, before
 // g): y = bf16(v g), or with swiglu the gated form of rows 2f / 2f + 1 held by
 // lanes 2i / 2i + 1 (every lane of the warp must call it).
@@ -222,20 +242,51 @@ __device__ __forceinline__ void f4_load_part(const F4Params &p, float (&part)[16
 
 // Sum of the parts of split row block rb for this thread's row r, in CTA
 // order ca..cb (fixed, so the result does not depend on which CTA adds it);
-// part `self` is `own`, the others come from the partial tiles.
+// part `self` is `own`, the others come from the partial tiles.  KQ float4 a
+// row hold the call's tokens; the loads of up to 8 / KQ parts are in flight
+// together (one memory round trip per batch).
+template <int KQ>
 __device__ __forceinline__ void f4_sum_parts(const F4Params &p, float (&sum)[16], int ca, int cb, int self,
                                              const float (&own)[16], int rb, int r, long long U, int KC) {
-    for (int c = ca; c <= cb; ++c) {
-        float part[16];
-        if (c == self) {
+    constexpr int B = 8 / KQ;
+    for (int c0 = ca; c0 <= cb; c0 += B) {
+        float4 f[B][KQ];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) part[t] = own[t];
-        } else {
-            f4_load_part(p, part, c, rb, r, U, KC);
+        for (int j = 0; j < B; ++j) {
+            const int c = c0 + j;
+            if (c <= cb && c != self) {
+                const long long cu0 = (long long)c * U / p.ctas;
+                const int crb0 = (int)(cu0 / KC);
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    p.partials + ((size_t)c * 2 + (rb == crb0 ? 0 : 1)) * (kUnitRows * 16) + (size_t)r * 16);
+#pragma unroll
+                for (int qd = 0; qd < KQ; ++qd) f[j][qd] = __ldcg(src + qd);
+            }
         }
 #pragma unroll
-        for (int t = 0; t < 16; ++t) sum[t] = c == ca ? part[t] : sum[t] + part[t];
+        for (int j = 0; j < B; ++j) {
+            const int c = c0 + j;
+            if (c > cb) break;
+#pragma unroll
+            for (int qd = 0; qd < KQ; ++qd) {
+                const float4 v = c == self ? make_float4(own[4 * qd], own[4 * qd + 1], own[4 * qd + 2], own[4 * qd + 3])
+                                           : f[j][qd];
+                if (c == ca) {
+                    sum[4 * qd] = v.x;
+                    sum[4 * qd + 1] = v.y;
+                    sum[4 * qd + 2] = v.z;
+                    sum[4 * qd + 3] = v.w;
+                } else {
+                    sum[4 * qd] += v.x;
+                    sum[4 * qd + 1] += v.y;
+                    sum[4 * qd + 2] += v.z;
+                    sum[4 * qd + 3] += v.w;
+                }
+            }
+        }
     }
+#pragma unroll
+    for (int t = 4 * KQ; t < 16; ++t) sum[t] = 0.f;
 }
 
 // Eight fp32 values -> eight E2M1 codes, value j in nibble j (the hardware
@@ -259,14 +310,14 @@ __device__ __forceinline__ uint32_t f4_cvt_e2m1x8(const float (&q)[8]) {
 
 // Shared memory: the ring (W + S tiles, plus the unit column's X codes when
 // they are streamed), the resident X codes (all K / 256 unit columns) when not,
-// the X block scales (per stage or all unit columns, like the codes), the
-// barriers, then flags and the term scales.
+// the X block scales of all unit columns, the barriers, then flags and the
+// term scales.
 int f4_smem_bytes(int stages, int cols, bool x_resident, int KC) {
     const int slot = f4_slot_bytes(cols), groups = (KC + kF4XGroup - 1) / kF4XGroup;
     const int xbars = x_resident ? (groups > stages ? groups : stages) : stages;
-    const int tabs = ((x_resident ? KC : stages) * f4_tab_bytes(cols) + 15) & ~15;
+    const int tabs = (KC * f4_tab_bytes(cols) + 15) & ~15;
     return stages * (kF4XOffHost + (x_resident ? 0 : slot)) + (x_resident ? KC * slot : 0) + tabs +
-           8 * (3 * stages + xbars + 8) + kF4MiscBytes;
+           8 * (3 * stages + xbars + 9) + kF4MiscBytes;
 }
 
 // TMEM: accumulators [issuer][segment buffer 2][f4_dstride(cols)] from column
@@ -280,6 +331,92 @@ int f4_max_stages(int cols, int smem_limit, bool x_resident, int KC) {
 }
 
 // ------------------------------------------------------------------ X prep
+// The expansion of one token's activations, shared by the X-prep kernel and
+// the GEMV's own prep (small n): the same arithmetic in both, so a token's
+// codes and scales do not depend on which of them wrote them.
+
+// Max |x| of bf16 values as bf16 magnitude bits (a uint32 max of the two halves).
+__device__ __forceinline__ uint32_t f4_absmax_bits(const uint4 &v, uint32_t m) {
+    m = __vmaxu2(m, v.x & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.w & 0x7FFF7FFFu);
+    return m;
+}
+
+// Term scales from the row's max |x| (bf16 magnitude bits; >= 0x7F80 is inf
+// or NaN, and the token's outputs become NaN): s_0 = max|x| / (6 * 2^8),
+// s_j = s_{j-1} / 6 (zero for an all-zero row).
+__device__ __forceinline__ void f4_term_scales(uint32_t m, float (&sc)[kF4Terms]) {
+    sc[0] = m < 0x7F80u ? __fdiv_rn(__uint_as_float(m << 16), 6.0f * kF4BlockHeadroom) : __int_as_float(0x7FC00000);
+#pragma unroll
+    for (int j = 1; j < kF4Terms; ++j) sc[j] = __fdiv_rn(sc[j - 1], 6.0f);
+}
+
+// Eight consecutive activations (this lane) of a 16-element block whose other
+// half the neighbouring lane (lane ^ 1) holds: the block exponent e and the
+// eight terms' E2M1 codes (code word j = term j, value i in nibble i).  Every
+// lane of the warp calls it.  The block scale b = 2^e is the smallest power of
+// two with 6 s_0 b >= the block's max |x|, within UE4M3's powers of two 2^-9
+// .. 2^8; rounding in the ratio can only pick the neighbouring power: a first
+// code clamped at 6 (the later terms take the excess) or one bit of the first
+// term unused.
+__device__ __forceinline__ int f4_expand8(const uint4 &raw, const float (&sc)[kF4Terms], bool finite,
+                                          uint32_t (&codes)[kF4Terms]) {
+    float r[8];
+    {
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            r[2 * i] = __uint_as_float(w[i] << 16);
+            r[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+    float bmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) bmax = fmaxf(bmax, fabsf(r[i]));
+    bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
+    int e = -9;
+    if (finite && sc[0] > 0.f) {
+        const float ratio = __fdiv_rn(bmax, 6.0f * sc[0]);
+        const uint32_t u = __float_as_uint(ratio);
+        const int E = (int)(u >> 23) - 127;  // ratio >= 0; 0 or subnormal give E = -127
+        if (ratio > 0.f) e = E + ((u & 0x7FFFFFu) != 0u ? 1 : 0);
+        e = min(max(e, -9), 8);
+    }
+    const float b = __int_as_float((e + 127) << 23);  // 2^e
+#pragma unroll
+    for (int j = 0; j < kF4Terms; ++j) {
+        codes[j] = 0;
+        const float sj = sc[j] * b;  // exact: a power-of-two multiple
+        if (finite && sj >= 1.17549435e-38f) {  // a subnormal scale's term is below any output's rounding
+            const float inv = __frcp_rn(sj);
+            float q[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q[i] = r[i] * inv;
+            codes[j] = f4_cvt_e2m1x8(q);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t h2 = e2m1x2_to_f16x2_rt(codes[j], i);
+                const float2 d = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+                r[2 * i] = fmaf(-d.x, sj, r[2 * i]);
+                r[2 * i + 1] = fmaf(-d.y, sj, r[2 * i + 1]);
+            }
+        }
+    }
+    return e;
+}
+
+// UE4M3 byte of 2^e (-9 <= e <= 8): subnormal below 2^-6.
+__device__ __forceinline__ uint8_t f4_ue4m3_pow2(int e) { return (uint8_t)(e >= -6 ? (e + 7) << 3 : 1 << (e + 9)); }
+
+// Byte offset of code word (column c, activations k0 .. k0 + 7) in a unit
+// column's code tile: row c of 128 bytes, 16-byte chunks swizzled by c % 8.
+__device__ __forceinline__ uint32_t f4_code_offset(int c, int k0) {
+    const int bo = (k0 & 255) >> 1;
+    return (uint32_t)(c * 128 + ((((bo >> 4) ^ (c & 7)) << 4) | (bo & 15)));
+}
+
 // Token t = blockIdx.y; this CTA expands activations [blockIdx.x * 2048,
 // + 2048) of it.  Every CTA of a token reads the whole row once (all loads in
 // flight together, one memory round trip) to find max |x| itself, so all of
@@ -303,12 +440,7 @@ __global__ void __maxnreg__(64) fp4_xprep_kernel(const uint16_t *__restrict__ x,
     const uint4 mine = own < nvec ? __ldg(xr + own) : make_uint4(0, 0, 0, 0);  // one of the above: same request
     uint32_t m = 0;
 #pragma unroll
-    for (int j = 0; j < L; ++j) {
-        m = __vmaxu2(m, v[j].x & 0x7FFF7FFFu);
-        m = __vmaxu2(m, v[j].y & 0x7FFF7FFFu);
-        m = __vmaxu2(m, v[j].z & 0x7FFF7FFFu);
-        m = __vmaxu2(m, v[j].w & 0x7FFF7FFFu);
-    }
+    for (int j = 0; j < L; ++j) m = f4_absmax_bits(v[j], m);
     m = max(m & 0xFFFFu, m >> 16);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -317,13 +449,9 @@ __global__ void __maxnreg__(64) fp4_xprep_kernel(const uint16_t *__restrict__ x,
     __syncthreads();
 #pragma unroll
     for (int w = 0; w < kF4XprepThreads / 32; ++w) m = max(m, wmax[w]);
-    // bf16 magnitude bits: >= 0x7F80 inf or NaN (the token's outputs become NaN)
     const bool finite = m < 0x7F80u;
-    // s_0 = max|x| / (6 * 2^8), s_j = s_{j-1} / 6 (zero for an all-zero row)
     float sc[kF4Terms];
-    sc[0] = finite ? __fdiv_rn(__uint_as_float(m << 16), 6.0f * kF4BlockHeadroom) : __int_as_float(0x7FC00000);
-#pragma unroll
-    for (int j = 1; j < kF4Terms; ++j) sc[j] = __fdiv_rn(sc[j - 1], 6.0f);
+    f4_term_scales(m, sc);
     if (blockIdx.x == 0 && tid < kF4Terms) {
 #pragma unroll
         for (int j = 0; j < kF4Terms; ++j)
@@ -331,60 +459,14 @@ __global__ void __maxnreg__(64) fp4_xprep_kernel(const uint16_t *__restrict__ x,
     }
     const int k0 = own * 8;
     if (k0 >= K) return;  // whole warps: K / 8 is a multiple of 32
-    float r[8];
-    {
-        const uint32_t w[4] = {mine.x, mine.y, mine.z, mine.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            r[2 * i] = __uint_as_float(w[i] << 16);
-            r[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-        }
-    }
-    // The 16-element block's scale b = 2^e (this thread and its neighbour hold
-    // the block): the smallest power of two with 6 s_0 b >= the block's max
-    // |x|, within UE4M3's powers of two 2^-9 .. 2^8.  Rounding in the ratio
-    // can only pick the neighbouring power: a first code clamped at 6 (the
-    // later terms take the excess) or one bit of the first term unused.
-    float bmax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) bmax = fmaxf(bmax, fabsf(r[i]));
-    bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
-    int e = -9;
-    if (finite && sc[0] > 0.f) {
-        const float ratio = __fdiv_rn(bmax, 6.0f * sc[0]);
-        const uint32_t u = __float_as_uint(ratio);
-        const int E = (int)(u >> 23) - 127;  // ratio >= 0; 0 or subnormal give E = -127
-        if (ratio > 0.f) e = E + ((u & 0x7FFFFFu) != 0u ? 1 : 0);
-        e = min(max(e, -9), 8);
-    }
-    const float b = __int_as_float((e + 127) << 23);  // 2^e
-    const int kc = k0 >> 8, bo = (k0 & 255) >> 1;
+    uint32_t codes[kF4Terms];
+    const int e = f4_expand8(mine, sc, finite, codes);
+    const int kc = k0 >> 8;
     uint8_t *const tile = xq + (size_t)kc * f4_slot_bytes(cols);
 #pragma unroll
-    for (int j = 0; j < kF4Terms; ++j) {
-        uint32_t codes = 0;
-        const float sj = sc[j] * b;  // exact: a power-of-two multiple
-        if (finite && sj >= 1.17549435e-38f) {  // a subnormal scale's term is below any output's rounding
-            const float inv = __frcp_rn(sj);
-            float q[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) q[i] = r[i] * inv;
-            codes = f4_cvt_e2m1x8(q);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t h2 = e2m1x2_to_f16x2_rt(codes, i);
-                const float2 d = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
-                r[2 * i] = fmaf(-d.x, sj, r[2 * i]);
-                r[2 * i + 1] = fmaf(-d.y, sj, r[2 * i + 1]);
-            }
-        }
-        const int c = t * kF4Terms + j;  // MMA column of (token, term): row c of the unit column's code tile
-        *reinterpret_cast<uint32_t *>(tile + c * 128 + ((((bo >> 4) ^ (c & 7)) << 4) | (bo & 15))) = codes;
-    }
-    // the block's UE4M3 byte: 2^e, subnormal below 2^-6
-    if ((own & 1) == 0)
-        xtab[(size_t)kc * f4_tab_bytes(cols) + t * 16 + ((k0 & 255) >> 4)] =
-            (uint8_t)(e >= -6 ? (e + 7) << 3 : 1 << (e + 9));
+    for (int j = 0; j < kF4Terms; ++j)  // MMA column of (token, term): row 8t + j of the unit column's code tile
+        *reinterpret_cast<uint32_t *>(tile + f4_code_offset(t * kF4Terms + j, k0)) = codes[j];
+    if ((own & 1) == 0) xtab[(size_t)kc * f4_tab_bytes(cols) + t * 16 + ((k0 & 255) >> 4)] = f4_ue4m3_pow2(e);
 }
 
 // Processing order of a CTA's units.  The CTA's range [u0, u0 + count) of the
@@ -478,17 +560,18 @@ __global__ void __maxnreg__(128)
     // the barriers
     const uint32_t kStage = kF4XOffHost + (xres ? 0u : kSlot);
     const uint32_t sX = sbase + S * kStage;                  // resident X codes
-    const uint32_t sTab = sX + (xres ? KC * kSlot : 0u);     // X block scales
+    const uint32_t sTab = sX + (xres ? KC * kSlot : 0u);     // X block scales of every unit column
     const int xgroups = (KC + kF4XGroup - 1) / kF4XGroup;    // bulk copies of resident X codes
     const int xbars = xres ? (xgroups > S ? xgroups : S) : S;
-    const uint32_t sFull = sTab + (((xres ? KC : S) * kTab + 15u) & ~15u);  // [S] W + S landed (TMA)
+    const uint32_t sFull = sTab + ((KC * kTab + 15u) & ~15u);  // [S] W + S landed (TMA)
     const uint32_t sXFull = sFull + 8 * S;      // [S] X codes of the stage landed / [xgroups] resident groups landed
     const uint32_t sSf = sXFull + 8 * xbars;    // [S] weight scales in tensor memory, count 4
     const uint32_t sEmpty = sSf + 8 * S;        // [S] MMAs done with the stage (commit)
     const uint32_t sDFull = sEmpty + 8 * S;     // [issuer][2] segment accumulated (commit)
     const uint32_t sDEmpty = sDFull + 32;       // [2] accumulators read, count 4
     const uint32_t sFinal = sDEmpty + 16;       // [issuer] every MMA done (commit)
-    const uint32_t sMisc = sFinal + 16;         // [0] tensor-memory base, [1] last-part flag, [2] preload flag,
+    const uint32_t sTabFull = sFinal + 16;      // the X block scales landed
+    const uint32_t sMisc = sTabFull + 8;        // [0] tensor-memory base, [1] last-part flag, [2] preload flag,
                                                 // [4 + q] units whose weight scales quarter q has stored
     uint32_t *const misc = reinterpret_cast<uint32_t *>(smem_raw + (sMisc - sbase));
     const uint32_t sSfDone = sMisc + 16;
@@ -525,6 +608,7 @@ __global__ void __maxnreg__(128)
         for (int b = 0; b < 4; ++b) mbar_init(sDFull + 8 * b, 1);
         for (int b = 0; b < 2; ++b) mbar_init(sDEmpty + 8 * b, 4);
         for (int b = 0; b < 2; ++b) mbar_init(sFinal + 8 * b, 1);
+        mbar_init(sTabFull, 1);
         for (int q = 0; q < 4; ++q) misc[4 + q] = 0;
         fence_barrier_init();
         if (count > 0) wk.begin(ord, S);
@@ -575,14 +659,15 @@ __global__ void __maxnreg__(128)
         if (lane == 0 && count > 0) {
             griddep_wait();  // the X codes are the output of the X-prep kernel ahead
             const uint64_t x_policy = l2_policy_evict_last();  // every CTA reads the same X codes
+            // every unit column's block scales first: the scale-factor warps need only these
+            mbar_arrive_expect_tx(sTabFull, KC * kTab);
+            bulk_load_f4(sTab, p.xtab, KC * kTab, sTabFull, x_policy);
             if (xres) {
-                // every unit column's X codes, kF4XGroup columns per bulk copy;
-                // all block scales with the first group
+                // every unit column's X codes, kF4XGroup columns per bulk copy
                 for (int g = 0; g < xgroups; ++g) {
                     const int c0 = g * kF4XGroup, nc = KC - c0 < kF4XGroup ? KC - c0 : kF4XGroup;
                     const uint32_t bytes = (uint32_t)nc * kSlot, bar = sXFull + 8 * g;
-                    mbar_arrive_expect_tx(bar, bytes + (g == 0 ? KC * kTab : 0u));
-                    if (g == 0) bulk_load_f4(sTab, p.xtab, KC * kTab, bar, x_policy);
+                    mbar_arrive_expect_tx(bar, bytes);
                     bulk_load_f4(sX + (uint32_t)c0 * kSlot, p.xq + (size_t)c0 * kSlot, bytes, bar, x_policy);
                 }
                 for (int g = 0; g < xgroups; ++g) {
@@ -601,10 +686,9 @@ __global__ void __maxnreg__(128)
                         break;
                     }
                     const uint32_t bar = sXFull + 8 * xw.st;
-                    mbar_arrive_expect_tx(bar, kSlot + kTab);
+                    mbar_arrive_expect_tx(bar, kSlot);
                     bulk_load_f4(sbase + xw.st * kStage + kF4XOffHost, p.xq + (size_t)xw.kc * kSlot, kSlot, bar,
                                  x_policy);
-                    bulk_load_f4(sTab + xw.st * kTab, p.xtab + (size_t)xw.kc * kTab, kTab, bar, x_policy);
                     xw.next();
                 }
                 const int lo = loaded > S ? loaded - S : 0;
@@ -615,6 +699,7 @@ __global__ void __maxnreg__(128)
                     }
                 }
             }
+            if (!mbar_wait_bounded(sTabFull, 0)) atomicOr(p.err, kDevErrTimeoutDrain);
         }
         __syncwarp();
     } else if (warp == kF4WarpIssuer || (kIssuers == 2 && warp == kF4WarpIssuer1)) {
@@ -707,22 +792,15 @@ __global__ void __maxnreg__(128)
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
         const int r = 32 * q + lane;
         bool ok = true;
-        if (xres && count > 0)  // every unit column's block scales land with the first X group
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(sXFull, 0));
-        F4Walk sw;
-        if (count > 0) sw.begin(ord, S);
-        for (int i = 0; i < count && ok; ++i, sw.next()) {
-            const int st = sw.st;
-            if (__any_sync(0xffffffffu, !mbar_wait_bounded(sFull + 8 * st, sw.ph) ||
-                                            (!xres && !mbar_wait_bounded(sXFull + 8 * st, sw.ph)))) {
-                ok = false;
-                break;
-            }
+        if (count > 0)  // every unit column's block scales, once
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(sTabFull, 0));
+        // one unit's two stores: the W scales of stage st, the X block scales of unit column kc
+        auto store_unit = [&](int st, int kc) {
             const uint32_t sfa = sf_base + st * kF4SfCols;
             const uint4 a = lds128(sbase + st * kStage + kF4WBytes + 16 * r);
             const uint32_t v[16] = {a.x, a.x, a.x, a.x, a.y, a.y, a.y, a.y, a.z, a.z, a.z, a.z, a.w, a.w, a.w, a.w};
             tc::st_32x32b_x16(sfa + lane_bits, v);
-            const uint32_t tab = sTab + (xres ? (uint32_t)sw.kc : (uint32_t)st) * kTab;
+            const uint32_t tab = sTab + (uint32_t)kc * kTab;
             uint32_t w[16];
 #pragma unroll
             for (int c32 = 0; c32 < 4; ++c32) {
@@ -735,13 +813,35 @@ __global__ void __maxnreg__(128)
                 w[12 + c32] = b.w;
             }
             tc::st_32x32b_x16(sfa + 16 + lane_bits, w);
+        };
+        // Units in pairs when the next stage has landed too: one hand-off
+        // (store wait, fence, arrivals) for both.
+        F4Walk sw;
+        if (count > 0) sw.begin(ord, S);
+        for (int i = 0; i < count && ok;) {
+            const int st0 = sw.st;
+            if (__any_sync(0xffffffffu, !mbar_wait_bounded(sFull + 8 * st0, sw.ph))) {
+                ok = false;
+                break;
+            }
+            store_unit(st0, sw.kc);
+            sw.next();
+            int done = 1;
+            if (i + 1 < count && __all_sync(0xffffffffu, mbar_test(sFull + 8 * sw.st, sw.ph))) {
+                store_unit(sw.st, sw.kc);
+                done = 2;
+            }
+            const int st1 = sw.st;
+            if (done == 2) sw.next();
             tc::wait_st();
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(sSf + 8 * st);
-                st_release_smem(sSfDone + 4 * q, (uint32_t)(i + 1));
+                mbar_arrive(sSf + 8 * st0);
+                if (done == 2) mbar_arrive(sSf + 8 * st1);
+                st_release_smem(sSfDone + 4 * q, (uint32_t)(i + done));
             }
+            i += done;
         }
         tc::wait_st();
         if (!ok && lane == 0) atomicOr(p.err, kDevErrTimeoutFull);
@@ -766,19 +866,37 @@ __global__ void __maxnreg__(128)
             const bool whole = len == KC;
             const long long ub = (long long)rb * KC;
             const int ca = (int)(((ub + 1) * p.ctas - 1) / U), cb = (int)(((ub + KC) * p.ctas - 1) / U);
-            // Before the last segment's accumulator is ready: if it is one of the
-            // two parts of a split row block and the other part is already
-            // published, load that now; this CTA then adds the last part and
-            // needs no count (a two-part sum is the same in either order).
+            const int sb = s & 1;
+            // While the last segment's MMAs run: if it is one of the two parts
+            // of a split row block, watch for the other part to be published
+            // and load it then; this CTA then adds the last part and needs no
+            // count (a two-part sum is the same in either order).  The watch
+            // ends when the accumulators are ready (bounded like every wait).
             if (s == ord.nseg - 1 && !whole && cb == ca + 1) {
-                if (warp == kF4WarpEpi0 && lane == 0) misc[2] = ld_acquire_u32(p.counters + rb) == 1u ? 1u : 0u;
-                named_sync(1, 128);
-                if (misc[2]) {
-                    pre_rb = rb;
-                    f4_load_part(p, pre_part, (int)blockIdx.x == ca ? cb : ca, rb, r, U, KC);
+                const unsigned long long t0 = globaltimer_ns();
+                for (;;) {
+                    if (warp == kF4WarpEpi0 && lane == 0) {
+                        unsigned v = ld_acquire_u32(p.counters + rb) == 1u ? 1u : 0u;
+                        if (!v) {
+                            bool ready = true;
+#pragma unroll
+                            for (int j = 0; j < kIssuers; ++j)
+                                ready = ready && mbar_test(sDFull + 8 * (j * 2 + sb), (s >> 1) & 1);
+                            v = ready || globaltimer_ns() - t0 > kWaitLimitNs ? 2u : 0u;
+                        }
+                        misc[2] = v;
+                    }
+                    named_sync(1, 128);
+                    const unsigned v = misc[2];
+                    named_sync(1, 128);  // misc[2] is written again in the next round
+                    if (v == 1u) {
+                        pre_rb = rb;
+                        f4_load_part(p, pre_part, (int)blockIdx.x == ca ? cb : ca, rb, r, U, KC);
+                    }
+                    if (v != 0u) break;
+                    __nanosleep(200);
                 }
             }
-            const int sb = s & 1;
             bool waited = true;
 #pragma unroll
             for (int j = 0; j < kIssuers; ++j)
@@ -865,15 +983,13 @@ __global__ void __maxnreg__(128)
                     if (4 * qd < p.n)
                         __stcg(reinterpret_cast<float4 *>(part_out) + qd,
                                make_float4(acc[4 * qd], acc[4 * qd + 1], acc[4 * qd + 2], acc[4 * qd + 3]));
-                __threadfence();
-                named_sync(1, 128);
+                named_sync(1, 128);  // every row's part is stored: one release covers them
                 if (warp == kF4WarpEpi0 && lane == 0) {
-                    const unsigned old = atomicAdd(p.counters + rb, 1u);
+                    const unsigned old = atom_add_acq_rel(p.counters + rb, 1u);
                     misc[1] = (old + 1 == (unsigned)(cb - ca + 1)) ? 1u : 0u;
                 }
                 named_sync(1, 128);
                 last = misc[1] != 0;
-                if (last) __threadfence();
             }
             if (!last) continue;
             float sum[16];
@@ -882,7 +998,7 @@ __global__ void __maxnreg__(128)
 #pragma unroll
                 for (int t = 0; t < 16; ++t) sum[t] = acc[t] + pre_part[t];
             } else {
-                f4_sum_parts(p, sum, ca, cb, (int)blockIdx.x, acc, rb, r, U, KC);
+                f4_sum_parts<(NC / kF4Terms + 3) / 4>(p, sum, ca, cb, (int)blockIdx.x, acc, rb, r, U, KC);
             }
             f4_store_row(p, sum, row, g);
             if (warp == kF4WarpEpi0 && lane == 0) p.counters[rb] = 0;  // ready for the next call
