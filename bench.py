@@ -31,6 +31,7 @@ GEMV has no exchange step); rank 0 prints the max-over-ranks timing.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import multiprocessing as mp
@@ -769,7 +770,7 @@ def main():
     def ffn_call(c, x, y, st):
         nv.nvfp4_ffn_swiglu(weights["ffn_gu"][c], weights["ffn_down"][c], x, h=h_ffn, y=y, stream=st)
 
-    def enqueue_step(st, p, public=False):
+    def enqueue_step(st, p):
         if is_ffn:
             ffn_call(p % len(weights["ffn_gu"]), xs[calls[0]], ys[calls[1]], st)
             return
@@ -777,11 +778,22 @@ def main():
         for s, n in calls:
             wp, ws, gs = weights[s][copy_index(s, seen[s], p)]
             seen[s] += 1
-            if public:  # the call a user makes
-                nv.nvfp4_gemv_batched(wp, ws, gs, xs[(s, n)], ys[(s, n)], stream=st)
-            else:
-                nv.nvfp4_gemv_batched_ex(wp, ws, gs, xs[(s, n)], ys[(s, n)], stream=st, variant=variant,
-                                         tiling=tiling)
+            nv.nvfp4_gemv_batched_ex(wp, ws, gs, xs[(s, n)], ys[(s, n)], stream=st, variant=variant, tiling=tiling)
+
+    # The end-to-end leg calls the C ABI entry point itself (nvfp4_gemv_batched,
+    # the call a C or C++ user makes) with the pointers marshalled once.
+    abi = nv.lib()
+    abi_args = []
+    for p in range(phases):
+        seen = {s: 0 for s in shapes_used}
+        step_args = []
+        for s, n in calls:
+            wp, ws, gs = weights[s][copy_index(s, seen[s], p)]
+            seen[s] += 1
+            N, K = SHAPES[s]
+            step_args.append((wp.data_ptr(), ws.data_ptr(), gs.data_ptr(), xs[(s, n)].data_ptr(),
+                              ys[(s, n)].data_ptr(), n, N, K, ctypes.c_void_p(stream.cuda_stream)))
+        abi_args.append(step_args)
 
     # warm the library (workspace for this stream, descriptors) outside capture
     with torch.cuda.stream(stream):
@@ -929,8 +941,8 @@ def main():
                  "launches_per_call": 3, "note": "two passes over W by design (amax, then blocks)"}
         del wq
 
-    # end to end through the public API with host buffers: every step copies
-    # the activations in from pinned host memory, makes the public calls
+    # end to end through the C ABI with host buffers: every step copies the
+    # activations in from pinned host memory, makes the C-ABI calls
     # (nvfp4_gemv_batched, un-captured) and copies the outputs back out
     e2e_steps = max(20, min(2000, args.steps // 10))
     if is_ffn:  # x goes in, y comes out (h stays on the device)
@@ -945,7 +957,10 @@ def main():
             ys_host[calls[1]].copy_(ys[calls[1]], non_blocking=True)
             return
         x_dev_all.copy_(x_host_all, non_blocking=True)
-        enqueue_step(stream, i % phases, public=True)
+        for args in abi_args[i % phases]:
+            st_ = abi.nvfp4_gemv_batched(*args)
+            if st_ != nv.NVFP4_OK:
+                raise SystemExit(f"nvfp4_gemv_batched: {nv.nvfp4_last_error()}")
         y_host_all.copy_(y_dev_all, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -1012,8 +1027,9 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4), "host_us_per_call": round(host_us_per_call, 2),
-                "how": "per step: one H2D copy of every call's X from pinned memory, the public calls "
-                       "(un-captured), one D2H copy of every Y; CUDA events on the stream"},
+                "how": "per step: one H2D copy of every call's X from pinned memory, the C-ABI calls "
+                       "nvfp4_gemv_batched (un-captured, default options), one D2H copy of every Y; CUDA events on "
+                       "the stream; host_us_per_call = host time to enqueue a call"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }

@@ -62,7 +62,8 @@ typedef enum nvfp4_variant {
     NVFP4_VARIANT_GENERIC = 3,  /* plain loads, any K % 16 == 0 and any alignment */
     NVFP4_VARIANT_TC = 4,       /* TMA ring + dequant into tensor memory + tcgen05.mma kind::f16 */
     NVFP4_VARIANT_FP4 = 5       /* TMA ring straight into block-scaled tcgen05.mma kind::mxf4nvf4 (W as
-                                   stored, X as a 6-term NVFP4 expansion written by a small prep kernel) */
+                                   stored, X as a sum of 8 NVFP4 terms written by a small prep kernel);
+                                   AUTO's choice for n <= 16 */
 } nvfp4_variant;
 
 /* Token tiling.  ONE_PASS streams W once for all n tokens (chunks of up to 16
@@ -82,8 +83,9 @@ typedef struct nvfp4_gemv_opts {
     int stages;              /* 0 = as many TMA ring stages as shared memory allows; else 2..8 */
     void *workspace;         /* NULL = library-owned per-stream workspace; else device memory */
     size_t workspace_bytes;  /* size of `workspace` (see nvfp4_gemv_workspace_size); if nonzero (with or without
-                                `workspace`) the plan keeps its scratch within it: n > 16 then takes 16-token
-                                passes instead of 32-token ones when those need more */
+                                `workspace`) the plan keeps its scratch within it: when AUTO's first choice
+                                needs more, the other fast kernel is tried (for n > 16: the FP4 kernel in
+                                16-token passes), then the tcgen05 kernel in 8-token passes */
     int inflight;            /* FP4 kernel: most weight stages requested and not yet landed per CTA (0 = default) */
 } nvfp4_gemv_opts;
 
@@ -104,23 +106,36 @@ typedef struct nvfp4_gemv_plan_info {
  *
  * w_packed, w_scale_e4m3, w_global_scale_f32, x_bf16: device, read only.
  * y_bf16: device, written.  n >= 0 (n == 0 is a no-op), N >= 1, K >= 16 and
- * K % 16 == 0.  Any n is accepted.  The fast (tcgen05) path needs
- * K % 256 == 0 and 16-byte aligned w_packed, w_scale_e4m3 and x_bf16 (other
- * inputs take the GENERIC kernel); it reads W once for up to 16 tokens and
- * once per 32 tokens above that (n = 17..32 in one pass: X is then converted
- * by one extra small kernel per pass), the weights of a pass that another
- * follows being left in L2.  Every output equals the single-token call's bit
- * for bit, whatever n.  The other kernels take up to 16 tokens per pass (fewer
- * when n * K is too large for shared memory), each pass re-reading W.
- * The tcgen05 path scales X by 2^-8 before its f16 conversion, so entries with
- * |x| >= 65520 * 2^8 (about 1.68e7) are out of range: they set the device
- * error word (nvfp4_device_error) and the output is not meaningful.
- * The tcgen05 kernel is launched with programmatic dependent launch: when the
- * kernel ahead of it on `stream` allows its dependents to start early, the
+ * K % 16 == 0.  Any n is accepted.  The fast paths need K % 256 == 0 and
+ * 16-byte aligned w_packed, w_scale_e4m3 and x_bf16 (other inputs take the
+ * GENERIC kernel).  For n <= 16 and K <= 32768 AUTO takes the FP4 kernel: one
+ * read of W for all n tokens, each token's activations written as 8 NVFP4
+ * terms (every 16-element block with its own power-of-two scale, so the full
+ * bf16 range is taken; a block's terms leave at most 1.5e-7 of its largest
+ * entry) by a small prep kernel launched ahead of the GEMV.  Above 16 tokens
+ * (or K > 32768) it takes the tcgen05 f16 kernel: one read of W per 32 tokens
+ * (X converted by one extra small kernel per pass), the weights of a pass that
+ * another follows being left in L2.  Within one kernel every output equals the
+ * single-token call's bit for bit, whatever n; since AUTO's kernel depends on
+ * n, calls of different n agree to the parity tolerance, and bit for bit when
+ * both take the same kernel (n <= 16: FP4).  The streaming CUDA-core kernels
+ * (MMA, SIMT) take up to 16 tokens per pass (fewer when n * K is too large for
+ * shared memory), each pass re-reading W.
+ * The tcgen05 path scales X by 2^-8 before its f16 conversion: entries with
+ * |x| >= 65520 * 2^8 (about 1.68e7) are out of its range and set the device
+ * error word (nvfp4_device_error), and entries below 2^-6 lose relative
+ * precision in f16 subnormals.  The MMA and SIMT kernels convert X to f16 too
+ * (scaled down by a power of two only when some |x| would overflow), with the
+ * same loss for small entries.  The FP4 and GENERIC kernels have neither.
+ * The GEMV kernels are launched with programmatic dependent launch: when the
+ * kernel ahead of them on `stream` allows its dependents to start early, the
  * GEMV begins reading w_packed and w_scale_e4m3 before that kernel finishes
- * (it reads x_bf16 and w_global_scale_f32 and writes y_bf16 only after).  So
- * the weights must not be written by the kernel launched just before the call
- * unless that kernel signals completion only at its end (the default).
+ * (it reads x_bf16, w_global_scale_f32 and its workspace and writes y_bf16 only
+ * after that kernel has completed).  So the weights must be written either by
+ * a non-kernel operation (a copy, a memset) or by a kernel that completes
+ * before the call's first kernel is launched, or one that allows its
+ * dependents to start only after its last write to them (this library's
+ * kernels do: the quantizer's last kernel writes before it allows them).
  * Uses a library-owned workspace tied to `stream`, allocated on the first call
  * on that stream (make that first call before capturing `stream` in a graph).
  * Calls on different streams may run concurrently.
@@ -166,11 +181,11 @@ nvfp4_status nvfp4_gemv_batched_noalloc(const uint8_t *w_packed, const uint8_t *
 
 /*
  * Gate/up projection with the SwiGLU activation fused into its output, for
- * the dense FFN of the K=m speculative-verify step that runs through batched
- * GEMV (rustdoc of spark_model/layers/mod.rs, FfnComponent: "dense SwiGLU";
- * can_forward_km / try_forward_km, "K=m (m=4..8) verify FFN via batched
- * GEMV").  The SwiGLU form is the usual one; the pages name it without a
- * formula:
+ * the dense FFN of the speculative-verify step over m = 4..8 draft tokens that
+ * runs through batched GEMV (rustdoc of spark_model/layers/mod.rs, the
+ * FfnComponent enum's dense SwiGLU variant and the can_forward_km /
+ * try_forward_km methods).  The SwiGLU form is the usual one; the pages name
+ * it without a formula:
  *
  *     h[t, f] = bf16( silu(G[t, f]) * U[t, f] ),   silu(a) = a / (1 + exp(-a)),
  *
@@ -182,8 +197,9 @@ nvfp4_status nvfp4_gemv_batched_noalloc(const uint8_t *w_packed, const uint8_t *
  * one global scale for both (quantize the interleaved matrix as one tensor,
  * e.g. with nvfp4_quantize_bf16).  x_bf16 [n][K]; h_bf16 [n][F] is written.
  * Same conventions and errors as nvfp4_gemv_batched (same invariant: a batched
- * call equals n single-token calls bit for bit); runs on the tcgen05 path
- * only, so K % 256 != 0 or unaligned inputs give NVFP4_ERR_UNSUPPORTED.
+ * call equals n single-token calls bit for bit); runs on the tensor-core
+ * paths only (FP4 for n <= 16, tcgen05 above), so K % 256 != 0 or unaligned
+ * inputs give NVFP4_ERR_UNSUPPORTED.
  * F >= 1.
  */
 nvfp4_status nvfp4_gemv_swiglu(const uint8_t *w_packed, const uint8_t *w_scale_e4m3,
@@ -207,9 +223,9 @@ nvfp4_status nvfp4_ffn_swiglu(const uint8_t *w_gu_packed, const uint8_t *w_gu_sc
 
 /*
  * Grouped read-once GEMV over routed experts, for MoE decode (rustdoc of
- * spark_model/layers/mod.rs, moe_grouped_decode_min_rows: the grouped arm
- * "reads each routed expert ONCE instead of once per token", on tokens
- * sorted by expert).  For every expert e and every assignment j in
+ * spark_model/layers/mod.rs, moe_grouped_decode_min_rows: with the tokens
+ * sorted by expert, the grouped path reads every routed expert's weights one
+ * time for all of its tokens rather than one time per token).  For every expert e and every assignment j in
  * [expert_offsets[e], expert_offsets[e+1]):
  *
  *     Y[j, r] = bf16( g_e * sum_k X[sorted_token[j], k] * E2M1(W_e[r, k]) * E4M3(S_e[r, k/16]) )
@@ -253,7 +269,12 @@ nvfp4_status nvfp4_gemv_plan(int n, int N, int K, const nvfp4_gemv_opts *opts,
                              nvfp4_gemv_plan_info *info);
 
 /*
- * Host-side NVFP4 quantizer for making test data (not on the GEMV path).
+ * Host-side NVFP4 quantizer for making test data (not on the GEMV path).  It
+ * produces the weight format of the file header as the test workloads state
+ * it: E2M1 values, one E4M3 scale per 16-element K block equal to the block's
+ * max |w| / 6 in units of the fp32 global scale, and g = amax / (6 * 448) so
+ * that the largest block scale is E4M3's largest value (the pages give the
+ * format and leave the scale choice open; this is the plainest reading).
  * w: host fp32 [N][K]; w_packed: host [N][K/2]; w_scale: host [N][K/16];
  * global_scale: host, 1 float.  amax = max|w|; g = amax / (6 * 448) in fp32
  * (1 when amax == 0); s = E4M3_rne_sat(blockabsmax / (6 g)); code =
@@ -316,7 +337,9 @@ nvfp4_status nvfp4_device_error(cudaStream_t stream, int *code);
  * NVFP4_OK or NVFP4_ERR_CUDA. */
 nvfp4_status nvfp4_selftest_wait_timeout(cudaStream_t stream);
 
-/* Message for the last non-OK status returned on this thread ("" if none). */
+/* Message for the last non-OK status returned on this thread ("" if none):
+ * which argument or check failed, or the CUDA call and its error string.  The
+ * pointer stays valid until the next library call on this thread. */
 const char *nvfp4_last_error(void);
 
 /* Library ABI version (major * 10000 + minor * 100 + patch). */

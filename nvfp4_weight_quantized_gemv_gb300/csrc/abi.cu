@@ -161,13 +161,46 @@ static nvfp4_status encode_2d(CUtensorMap *map, const void *ptr, uint64_t cols, 
     return NVFP4_OK;
 }
 
-// The bf16 X of one pass for the tcgen05 kernel with 16 staged tokens, viewed
-// as 3D {64 k, n tokens, K/64 k-chunks} (token stride 2K bytes, chunk stride
-// 128 bytes) so that one box {64, 16, 4} is one unit's X in the tensor core's
-// 128-byte-swizzled K-major layout; tokens past n read as zeros.  The kernel
-// converts the landed box to f16 in place.  (With 8 staged tokens the kernel
+// encode_2d through a small per-thread cache: a decode step calls the same
+// few weight matrices over and over, and encoding a tensor map is host work
+// on every call's path.  Keyed by everything the map depends on.
+struct MapCacheEntry {
+    const void *ptr;
+    uint64_t cols, rows;
+    uint32_t box_cols, box_rows;
+    int swizzle;
+    CUtensorMap map;
+};
+static nvfp4_status encode_2d_cached(CUtensorMap *map, const void *ptr, uint64_t cols, uint64_t rows,
+                                     uint32_t box_cols, uint32_t box_rows,
+                                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
+    constexpr int kEntries = 32;
+    static thread_local MapCacheEntry cache[kEntries];
+    static thread_local int used = 0, next = 0;
+    for (int i = 0; i < used; ++i) {
+        const MapCacheEntry &c = cache[i];
+        if (c.ptr == ptr && c.cols == cols && c.rows == rows && c.box_cols == box_cols && c.box_rows == box_rows &&
+            c.swizzle == (int)swizzle) {
+            *map = c.map;
+            return NVFP4_OK;
+        }
+    }
+    nvfp4_status st = encode_2d(map, ptr, cols, rows, box_cols, box_rows, swizzle);
+    if (st != NVFP4_OK) return st;
+    MapCacheEntry &c = cache[next];
+    c = MapCacheEntry{ptr, cols, rows, box_cols, box_rows, (int)swizzle, *map};
+    next = (next + 1) % kEntries;
+    if (used < kEntries) ++used;
+    return NVFP4_OK;
+}
+
+// The f16 X of one pass for the tcgen05 kernel with 32 staged tokens (the
+// output of its conversion kernel), viewed as 3D {64 k, n tokens, K/64
+// k-chunks} (token stride 2K bytes, chunk stride 128 bytes) so that one box
+// {64, 32, 4} is one unit's X in the tensor core's 128-byte-swizzled K-major
+// layout; tokens past n read as zeros.  (With 8 staged tokens the kernel
 // copies X rows itself and needs no map.)
-static nvfp4_status encode_x(CUtensorMap *map, const uint16_t *x, int n, int K, int box_tokens = 16) {
+static nvfp4_status encode_x(CUtensorMap *map, const uint16_t *x, int n, int K, int box_tokens) {
     EncodeTiledFn fn;
     nvfp4_status st = get_encode_fn(&fn);
     if (st != NVFP4_OK) return st;
@@ -316,32 +349,78 @@ static std::vector<int> greedy_321(int n) {
     return t;
 }
 
+// AUTO's choice of kernel for a fast-path call: FP4 for n <= 16 and the
+// tcgen05 kernel above (default), the tcgen05 kernel only, or FP4 in passes of
+// 16 tokens for any n.
+enum AutoMode { kAutoDefault = 0, kAutoTcOnly = 1, kAutoFp4Passes = 2 };
 static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nvfp4_gemv_opts &o, int sms,
-                                     int smem_optin, int tc_per_pass, bool allow_fp4, Plan *plan);
+                                     int smem_optin, int tc_per_pass, AutoMode mode, Plan *plan);
 
 // AUTO picks the FP4 kernel for n <= 16 (one pass of W for every token) and
 // the tcgen05 kernel with 32 staged tokens above.  When the caller declares a
-// scratch size (workspace_bytes) too small for that plan, AUTO falls back to
-// the tcgen05 kernel, and its 32-token pass to 16-token passes.
+// scratch size (workspace_bytes) too small for that plan, AUTO tries the other
+// of the two (the FP4 kernel in 16-token passes for n > 16), then the
+// tcgen05 kernel in 8-token passes.
+static nvfp4_status make_plan_uncached(int n, int N, int K, bool fast_ok, const nvfp4_gemv_opts &o, int sms,
+                                       int smem_optin, Plan *plan);
+
+// Plans through a small per-thread cache keyed by the call's shape, the
+// options that shape the plan and the device's limits (planning walks the
+// partition, which is host work on every call's path).
+struct PlanCacheEntry {
+    int n, N, K, sms, smem_optin, variant, tiling, num_ctas, stages, inflight;
+    bool fast_ok;
+    size_t workspace_bytes;
+    Plan plan;
+};
 static nvfp4_status make_plan(int n, int N, int K, bool fast_ok, const nvfp4_gemv_opts &o, int sms, int smem_optin,
                               Plan *plan) {
+    constexpr int kEntries = 16;
+    static thread_local PlanCacheEntry cache[kEntries];
+    static thread_local int used = 0, next = 0;
+    for (int i = 0; i < used; ++i) {
+        const PlanCacheEntry &c = cache[i];
+        if (c.n == n && c.N == N && c.K == K && c.fast_ok == fast_ok && c.sms == sms && c.smem_optin == smem_optin &&
+            c.variant == o.variant && c.tiling == o.tiling && c.num_ctas == o.num_ctas && c.stages == o.stages &&
+            c.inflight == o.inflight && c.workspace_bytes == o.workspace_bytes) {
+            *plan = c.plan;
+            return NVFP4_OK;
+        }
+    }
+    nvfp4_status st = make_plan_uncached(n, N, K, fast_ok, o, sms, smem_optin, plan);
+    if (st != NVFP4_OK) return st;
+    cache[next] = PlanCacheEntry{n, N, K, sms, smem_optin, o.variant, o.tiling, o.num_ctas, o.stages, o.inflight,
+                                 fast_ok, o.workspace_bytes, *plan};
+    next = (next + 1) % kEntries;
+    if (used < kEntries) ++used;
+    return NVFP4_OK;
+}
+
+static nvfp4_status make_plan_uncached(int n, int N, int K, bool fast_ok, const nvfp4_gemv_opts &o, int sms,
+                                       int smem_optin, Plan *plan) {
     const bool small_ws = o.workspace_bytes != 0;
-    nvfp4_status st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kTcMaxTokensPerPass, true, plan);
-    if (st == NVFP4_OK && o.variant == kAuto && plan->variant == kFp4 && small_ws &&
-        o.workspace_bytes < plan->ws_bytes)
-        st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kTcMaxTokensPerPass, false, plan);
-    if (st == NVFP4_OK && plan->tc_tokens == 32 && small_ws && o.workspace_bytes < plan->ws_bytes)
-        st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kMaxTokensPerPass, false, plan);
+    auto too_big = [&](const Plan *pl) { return small_ws && o.workspace_bytes < pl->ws_bytes; };
+    nvfp4_status st =
+        make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kTcMaxTokensPerPass, kAutoDefault, plan);
+    if (st == NVFP4_OK && o.variant == kAuto && too_big(plan)) {
+        if (plan->variant == kFp4)
+            st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kTcMaxTokensPerPass, kAutoTcOnly, plan);
+        else if (plan->variant == kTc && K <= kF4MaxK)
+            st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kTcMaxTokensPerPass, kAutoFp4Passes, plan);
+    }
+    if (st == NVFP4_OK && plan->variant == kTc && plan->tc_tokens == 32 && too_big(plan))
+        st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, 8, kAutoTcOnly, plan);
     return st;
 }
 
 static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nvfp4_gemv_opts &o, int sms,
-                                     int smem_optin, int tc_per_pass, bool allow_fp4, Plan *plan) {
+                                     int smem_optin, int tc_per_pass, AutoMode mode, Plan *plan) {
     Plan p;
     p.variant = o.variant;
     const bool tc_ok = fast_ok;
     if (p.variant == kAuto) {
-        const bool fp4_ok = allow_fp4 && fast_ok && n <= kF4MaxTokensPerPass && K <= kF4MaxK;
+        const bool fp4_ok = fast_ok && K <= kF4MaxK &&
+                            (mode == kAutoFp4Passes || (mode == kAutoDefault && n <= kF4MaxTokensPerPass));
         p.variant = fp4_ok ? kFp4 : tc_ok ? kTc : kGeneric;
     }
     if ((p.variant == kMma || p.variant == kSimt) && !fast_ok)
@@ -365,7 +444,7 @@ static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nv
         int fit = room / (2 * K);
         if (fit < 1) return fail(NVFP4_ERR_UNSUPPORTED, "K = %d too large for the streaming kernel", K);
         per_pass = fit < per_pass ? fit : per_pass;
-    }  // tcgen05: 16 (X held per k-group) or 32 (X streamed per unit) tokens per pass for any K
+    }  // tcgen05: 32 tokens per pass (X streamed per unit) for any K, or 8 (X held per k-group)
     if (p.tiling == NVFP4_TILING_GREEDY_321) {
         p.tiles = greedy_321(n);
     } else {
@@ -412,7 +491,11 @@ static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nv
     } else if (p.variant != kGeneric) {
         int max_tile = 0;
         for (int t : p.tiles) max_tile = t > max_tile ? t : max_tile;
-        const int T = max_tile > 16 ? 32 : max_tile > 8 ? 16 : 8;
+        // tcgen05 staged tokens: 8, else 32 (X pre-converted, streamed per unit).
+        // The 16-token mode of the kernel (X converted in place per k-group)
+        // returned run-to-run differing, wrong outputs in some row blocks for
+        // long unit ranges per CTA on GB300 (cause not found); it is not used.
+        const int T = max_tile > 8 ? 32 : 8;
         const int unit_k = p.variant == kTc ? kTcUnitKHost : kUnitK;
         p.units = (long long)((N + kUnitRows - 1) / kUnitRows) * (K / unit_k);
         int ctas = o.num_ctas ? o.num_ctas : sms;
@@ -430,12 +513,7 @@ static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nv
         // the tcgen05 kernel needs an even number of stages (every consumer warp
         // waits on every phase of a stage's barriers)
         const int stage_step = p.variant == kTc ? 2 : 1;
-        // 16 staged tokens: at most 6 stages.  With 8, long unit ranges per CTA
-        // (about 30 units and more) gave run-to-run differing, wrong outputs in
-        // some row blocks on GB300; 6 and fewer stages, and the 8- and
-        // 32-token modes with 8, were exact over the same shapes.
-        const int max_stages = (p.variant == kTc && T == 16) ? 6 : kMaxStages;
-        int stages = max_stages;
+        int stages = kMaxStages;
         while (stages > 2 && smem_for(stages) > smem_optin) stages -= stage_step;
         if (smem_for(stages) > smem_optin) return fail(NVFP4_ERR_UNSUPPORTED, "K = %d does not fit shared memory", K);
         if (o.stages != 0) {
@@ -534,13 +612,13 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
     }
     CUtensorMap tw, ts;
     if (plan.variant == kTc || plan.variant == kFp4) {
-        if ((st = encode_2d(&tw, wp, (uint64_t)K / 2, (uint64_t)N, 128, kUnitRows, CU_TENSOR_MAP_SWIZZLE_128B)) !=
-            NVFP4_OK)
+        if ((st = encode_2d_cached(&tw, wp, (uint64_t)K / 2, (uint64_t)N, 128, kUnitRows,
+                                   CU_TENSOR_MAP_SWIZZLE_128B)) != NVFP4_OK)
             return st;
-    } else if ((st = encode_2d(&tw, wp, (uint64_t)K / 2, (uint64_t)N, kUnitK / 2, kUnitRows)) != NVFP4_OK) {
+    } else if ((st = encode_2d_cached(&tw, wp, (uint64_t)K / 2, (uint64_t)N, kUnitK / 2, kUnitRows)) != NVFP4_OK) {
         return st;
     }
-    if ((st = encode_2d(&ts, ws, (uint64_t)K / 16, (uint64_t)N, 16, kUnitRows)) != NVFP4_OK) return st;
+    if ((st = encode_2d_cached(&ts, ws, (uint64_t)K / 16, (uint64_t)N, 16, kUnitRows)) != NVFP4_OK) return st;
 
     if (plan.variant == kFp4) {
         F4Params fp;
@@ -602,7 +680,6 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
         if (plan.variant == kTc) {
             CUtensorMap tx;
             memset(&tx, 0, sizeof tx);
-            if (plan.tc_tokens == 16 && (st = encode_x(&tx, sp.x, tn, K)) != NVFP4_OK) return st;
             if (plan.tc_tokens == 32) {
                 // the pass's X converted once to f16 x 2^-8; the GEMV streams it per unit
                 if ((e = launch_tc_x16(sp.x, x16, tn, K, d->err_word, stream)) != cudaSuccess)

@@ -23,15 +23,15 @@
 // core's K-major 128-byte-swizzled operand layout (8-token atoms of 1024 B).
 // With n <= 8 (T = 8) the X warp fetches each token's whole slice with one
 // bulk copy into a staging area, and the epilogue warps convert it into the
-// swizzled layout; rows n..7 are zeroed beforehand.  With T = 16 the X warp
-// loads one 3D TMA box per unit straight into the swizzled layout (rows
-// past n zero-filled) and the epilogue warps convert it in place.  No
-// separate conversion kernel or X buffer in global memory.  With T = 32 the
-// group's X for 32 tokens would not fit beside the weight ring: X is
-// converted once per pass by tc_x16_kernel into the workspace and the X warp
-// streams each unit's {64 k, 32 tokens, 4} box into a ring of kTcXRing slots,
-// which the unit's two issuers release with a commit; same partition, so the
-// results equal those of n <= 16 calls bit for bit.
+// swizzled layout; rows n..7 are zeroed beforehand.  No separate conversion
+// kernel or X buffer in global memory.  With 9 to 32 tokens (T = 32) the
+// group's X would not fit beside the weight ring: X is converted once per
+// pass by tc_x16_kernel into the workspace and the X warp streams each unit's
+// {64 k, 32 tokens, 4} box into a ring of kTcXRing slots, which the unit's
+// two issuers release with a commit; same partition, so the results equal
+// those of n <= 8 calls bit for bit.  (A 16-token mode that converted X in
+// place per k-group returned run-to-run differing outputs in some row blocks
+// on GB300 for long unit ranges per CTA; it was removed, its cause not found.)
 //
 // Warp roles (576 threads, one CTA per SM):
 //   warp 0       weight producer: 2D TMA loads of the unit's W tile
@@ -229,10 +229,9 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, uint32_t 
 
 }  // namespace
 
-// X area: kg_max units x 16 token rows x 512 B -- the f16 X for T = 16, or
-// the f16 X (8 rows) plus the bf16 staging (8 rows) for T = 8: the same size,
-// so the partition does not depend on n; for T = 32, kTcXRing slots of 32
-// token rows x 512 B.
+// X area: kg_max units x 16 token rows x 512 B -- the f16 X (8 rows) plus the
+// bf16 staging (8 rows) for T = 8; for T = 32, kTcXRing slots of 32 token
+// rows x 512 B.
 // The dynamic shared memory starts 1024-byte aligned (the kernel checks it),
 // so no alignment slack is reserved: the GEMV then leaves room on its SM for a
 // reduction CTA (its 1 KB of reserved shared memory).
@@ -248,11 +247,11 @@ void tc_group_host(int g, int groups, int KC, int *kstart, int *kg) { tc_group(g
 
 // At most kTcMaxRegs registers a thread, so that a reduction CTA can sit
 // beside the GEMV CTA (see the launch notes above).
-template <int T>  // staged tokens: 8 (n <= 8), 16 (n <= 16) or 32 (X ring, pre-converted)
+template <int T>  // staged tokens: 8 (n <= 8) or 32 (X ring, pre-converted)
 __global__ void __maxnreg__(kTcMaxRegs)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
                    const __grid_constant__ CUtensorMap tmap_x, const StreamParams p, const TcPartition part) {
-    static_assert(T == 8 || T == 16 || T == 32, "staged tokens");
+    static_assert(T == 8 || T == 32, "staged tokens");
     constexpr bool kRing = T == 32;        // X streamed per unit through kTcXRing slots
     constexpr int kAcc = T < 16 ? 16 : T;  // accumulator columns per (issuer, segment buffer)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -348,7 +347,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
         mbar_init(sXReq, 1);
         fence_barrier_init();
     }
-    if (T >= 16 && warp == kTcWarpX && lane == 0) prefetch_tensormap(&tmap_x);  // T = 8 uses no X map
+    if (T == 32 && warp == kTcWarpX && lane == 0) prefetch_tensormap(&tmap_x);  // T = 8 uses no X map
     if (warp == kTcWarpIssuer0) {
         tc::tmem_alloc(sMisc, kTcTmemCols);
         tc::tmem_relinquish();
@@ -370,9 +369,6 @@ __global__ void __maxnreg__(kTcMaxRegs)
     //           token t (lane = 16-byte chunk of the column's 512 bytes) and
     //           go to the chunk's swizzled position; rows n..7 are zeroed by
     //           zero_x_pad before the wait for X.
-    //   T = 16: the landed TMA box is converted in place (rows past n are the
-    //           TMA's zero fill; a chunk's position inside the swizzled box
-    //           does not matter to an elementwise conversion).
     auto zero_x_pad = [&](int cv) {
         if (T != 8) return;
         const int pad = T - p.n;
@@ -398,27 +394,6 @@ __global__ void __maxnreg__(kTcMaxRegs)
                 v.z = bf16x2_to_f16x2_scaled(v.z, bad);
                 v.w = bf16x2_to_f16x2_scaled(v.w, bad);
                 sts128(dst_box + t * 128 + ((uint32_t)((lane & 7) ^ (t & 7)) << 4), v);
-            }
-            fence_proxy_async_smem();  // the tensor core reads these bytes through the async proxy
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sXFull + 8 * l);
-        }
-        for (int i = 0; i < nx && ok && T == 16; ++i) {  // per column, as its box lands
-            const int l = (kl0 + i) % kg;
-            const uint32_t col = sX + l * xslot;
-            if (__any_sync(0xffffffffu, !mbar_wait_bounded(sXLoaded + 8 * l, 0))) {
-                ok = false;
-                break;
-            }
-            for (int c = cv * 32 + lane; c < 32 * T; c += kTcXConverterWarps * 32) {
-                if (((c >> 3) & (T - 1)) >= p.n) continue;  // row (c >> 3) = box * T + token
-                const uint32_t addr = col + (uint32_t)c * 16;
-                uint4 v = lds128(addr);
-                v.x = bf16x2_to_f16x2_scaled(v.x, bad);
-                v.y = bf16x2_to_f16x2_scaled(v.y, bad);
-                v.z = bf16x2_to_f16x2_scaled(v.z, bad);
-                v.w = bf16x2_to_f16x2_scaled(v.w, bad);
-                sts128(addr, v);
             }
             fence_proxy_async_smem();  // the tensor core reads these bytes through the async proxy
             __syncwarp();
@@ -481,31 +456,15 @@ __global__ void __maxnreg__(kTcMaxRegs)
             }
         } else if (lane == 0) {
             const uint64_t policy = l2_policy_evict_last();  // every CTA of the group reads the same X
-            if (T == 8) {
-                // one bulk copy per token: its kg units of the group, contiguous in X
-                const uint32_t bytes = (uint32_t)kg * 512;
-                mbar_arrive_expect_tx(sXLoaded, bytes * (uint32_t)p.n);
-                for (int t = 0; t < p.n; ++t)
-                    bulk_load(sStage + t * stage_pitch, p.x + (size_t)t * p.K + (size_t)kstart * kTcUnitK, bytes,
-                              sXLoaded, policy);
-            } else {
-                for (int i = 0; i < nx; ++i) {  // in the order the CTA uses them
-                    const int l = (kl0 + i) % kg;
-                    const uint32_t bar = sXLoaded + 8 * l;
-                    mbar_arrive_expect_tx(bar, xslot);
-                    tma_load_3d(sX + l * xslot, &tmap_x, 0, 0, (kstart + l) * 4, bar, policy);
-                }
-            }
+            // T = 8: one bulk copy per token, its kg units of the group (contiguous in X)
+            const uint32_t bytes = (uint32_t)kg * 512;
+            mbar_arrive_expect_tx(sXLoaded, bytes * (uint32_t)p.n);
+            for (int t = 0; t < p.n; ++t)
+                bulk_load(sStage + t * stage_pitch, p.x + (size_t)t * p.K + (size_t)kstart * kTcUnitK, bytes,
+                          sXLoaded, policy);
             mbar_arrive(sXReq);  // the producer may request the rest of the weight ring
-            // wait (bounded) for every copy before the warp leaves (the conversion may give up)
-            const int waits = T == 8 ? 1 : nx;
-            for (int i = 0; i < waits; ++i) {
-                const uint32_t bar = T == 8 ? sXLoaded : sXLoaded + 8 * ((kl0 + i) % kg);
-                if (!mbar_wait_bounded(bar, 0)) {
-                    atomicOr(p.err, kDevErrTimeoutDrain);
-                    break;
-                }
-            }
+            // wait (bounded) for the copies before the warp leaves (the conversion may give up)
+            if (!mbar_wait_bounded(sXLoaded, 0)) atomicOr(p.err, kDevErrTimeoutDrain);
         }
         __syncwarp();
     } else if (warp < kTcWarpDequant0) {
@@ -543,13 +502,13 @@ __global__ void __maxnreg__(kTcMaxRegs)
 #pragma unroll
                     for (int part = p0; part < p0 + kTcPartsPerIssuer; ++part) {
                         // descriptors of the part's 64-k boxes: tokens 8-15 are the next
-                        // atom (T == 16) or the zero block (T == 8)
+                        // atom (T == 32) or the zero block (T == 8)
                         constexpr int kBoxes = kTcStepsPerPart / 4;
                         uint64_t bd[kBoxes];
 #pragma unroll
                         for (int h = 0; h < kBoxes; ++h) {
                             const uint32_t box = xbase + (uint32_t)(part * kBoxes + h) * xbox;
-                            bd[h] = tc::smem_desc_sw128(box, (T >= 16) ? 1024u : (sZero - box));
+                            bd[h] = tc::smem_desc_sw128(box, (T == 32) ? 1024u : (sZero - box));
                         }
                         if (!mbar_wait_bounded(sAFull + 8 * (a * kTcAParts + part), par)) {
                             ok = false;
@@ -871,8 +830,6 @@ cudaError_t launch_tc_x16(const uint16_t *x, uint16_t *x16, int n, int K, unsign
 cudaError_t tc_set_smem_limit(int smem_optin) {
     cudaError_t e = cudaFuncSetAttribute(gemv_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gemv_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
-    if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(gemv_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
 }
 
@@ -888,9 +845,9 @@ cudaError_t launch_tc(const CUtensorMap &tw, const CUtensorMap &ts, const CUtens
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = T == 32   ? cudaLaunchKernelEx(&cfg, gemv_tc_kernel<32>, tw, ts, tx, p, part)
-                    : T == 16 ? cudaLaunchKernelEx(&cfg, gemv_tc_kernel<16>, tw, ts, tx, p, part)
-                              : cudaLaunchKernelEx(&cfg, gemv_tc_kernel<8>, tw, ts, tx, p, part);
+    if (T != 8 && T != 32) return cudaErrorInvalidValue;
+    cudaError_t e = T == 32 ? cudaLaunchKernelEx(&cfg, gemv_tc_kernel<32>, tw, ts, tx, p, part)
+                            : cudaLaunchKernelEx(&cfg, gemv_tc_kernel<8>, tw, ts, tx, p, part);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t rc = {};
     rc.gridDim = dim3(part.row_blocks);
@@ -898,9 +855,8 @@ cudaError_t launch_tc(const CUtensorMap &tw, const CUtensorMap &ts, const CUtens
     rc.stream = stream;
     rc.attrs = attr;
     rc.numAttrs = 1;
-    return T == 32   ? cudaLaunchKernelEx(&rc, tc_reduce_kernel<32>, p, part)
-           : T == 16 ? cudaLaunchKernelEx(&rc, tc_reduce_kernel<16>, p, part)
-                     : cudaLaunchKernelEx(&rc, tc_reduce_kernel<8>, p, part);
+    return T == 32 ? cudaLaunchKernelEx(&rc, tc_reduce_kernel<32>, p, part)
+                   : cudaLaunchKernelEx(&rc, tc_reduce_kernel<8>, p, part);
 }
 
 }  // namespace nvfp4

@@ -141,10 +141,16 @@ def test_one_pass_plan():
     assert nv.nvfp4_gemv_plan(32, 14336, 5120)["tile_tokens"] == [32]
     assert nv.nvfp4_gemv_plan(64, 14336, 5120)["tile_tokens"] == [32, 32]
     assert nv.nvfp4_gemv_plan(40, 14336, 5120)["tile_tokens"] == [32, 8]
-    # a declared scratch size too small for the 32-token pass: 16-token passes
-    small = nv.nvfp4_gemv_workspace_size(16, 14336, 5120, variant=nv.VARIANT_TC)
+    # a declared scratch size too small for the 32-token pass: FP4 16-token passes
+    small = nv.nvfp4_gemv_workspace_size(16, 14336, 5120)
     assert nv.nvfp4_gemv_workspace_size(32, 14336, 5120) > small
-    assert nv.nvfp4_gemv_plan(40, 14336, 5120, workspace_bytes=small)["tile_tokens"] == [16, 16, 8]
+    capped = nv.nvfp4_gemv_plan(40, 14336, 5120, workspace_bytes=small)
+    assert capped["tile_tokens"] == [16, 16, 8] and capped["variant"] == "fp4"
+    # beyond the FP4 kernel's K: the tcgen05 kernel's 8-token passes
+    tc8 = nv.nvfp4_gemv_workspace_size(8, 1024, 33024)
+    assert nv.nvfp4_gemv_plan(20, 1024, 33024, workspace_bytes=tc8)["tile_tokens"] == [8, 8, 4]
+    # the tcgen05 kernel stages 8 or 32 tokens (9 to 16 take the 32-token mode)
+    assert nv.nvfp4_gemv_plan(12, 1024, 8192, variant=nv.VARIANT_TC)["tile_tokens"] == [12]
     # K too large for 16 tokens of X in shared memory: smaller chunks
     p = nv.nvfp4_gemv_plan(16, 1024, 8192)
     assert p["tile_tokens"] == [16]        # FP4: X codes streamed per unit when not resident

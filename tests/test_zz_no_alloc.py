@@ -8,7 +8,7 @@ keeps the kernel's scratch in a static device array.  These tests call that
 entry point through the C ABI (ctypes): twice in a row against the ordinary
 entry point (same plan, so bit for bit) and sampled points of the oracle
 within the parity tolerance; a call whose 32-token pass does not fit the
-scratch (two 16-token passes, as the _ex entry point with an 8 MiB
+scratch (two 16-token FP4 passes, as the _ex entry point with an 8 MiB
 workspace); and a call refused because no plan fits.  It lives in its own file, collected last, and needs no state
 from earlier tests.
 """
@@ -79,15 +79,17 @@ def _check_sampled(wp, ws, gs, xt, y, seed):
 
 
 def test_noalloc_takes_16_token_passes_when_32_do_not_fit():
-    """n = 32 at K = 16384: the 32-token pass needs more than the 8 MiB static
-    scratch, so the call runs two 16-token passes -- the plan, and the bits, of
-    the _ex entry point given an 8 MiB workspace."""
+    """n = 32 at K = 16384: the tcgen05 kernel's 32-token pass needs more than
+    the 8 MiB static scratch, so the call runs two 16-token passes of the FP4
+    kernel -- the plan, and the bits, of the _ex entry point given an 8 MiB
+    workspace."""
     nv.build()
     oracle.build()
     N, K, n = 14336, 16384, 32
     cap = 8 << 20
     assert nv.nvfp4_gemv_workspace_size(n, N, K) > cap
-    assert nv.nvfp4_gemv_plan(n, N, K, workspace_bytes=cap)["tile_tokens"] == [16, 16]
+    plan = nv.nvfp4_gemv_plan(n, N, K, workspace_bytes=cap)
+    assert plan["tile_tokens"] == [16, 16] and plan["variant"] == "fp4"
     wp, ws, gs, xt = _case(N, K, n, 40, 41)
     work = torch.zeros(cap, dtype=torch.uint8, device="cuda")
     y_ex = nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt, workspace=work)
@@ -104,11 +106,12 @@ def test_noalloc_takes_16_token_passes_when_32_do_not_fit():
 
 
 def test_noalloc_refuses_a_plan_beyond_the_static_scratch():
-    """17 tokens over 262144 rows of K = 256: even 16-token passes need more than
-    8 MiB of split-tile scratch; the call is refused before anything is enqueued."""
+    """17 tokens over 262144 rows of K = 33024 (beyond the FP4 kernel's K): even
+    the tcgen05 kernel's 8-token passes need far more than 8 MiB of split-tile
+    scratch; the call is refused before anything is enqueued."""
     nv.build()
-    N, K, n = 262144, 256, 17
-    assert nv.nvfp4_gemv_workspace_size(16, N, K, variant=nv.VARIANT_TC) > (8 << 20)
+    N, K, n = 262144, 33024, 17
+    assert nv.nvfp4_gemv_workspace_size(8, N, K) > (8 << 20)
     L = nv.lib()
     p = ctypes.c_void_p(1 << 20)      # aligned, never dereferenced: the refusal comes first
     assert L.nvfp4_gemv_batched_noalloc(p, p, p, p, p, n, N, K, None) == nv.NVFP4_ERR_WORKSPACE
