@@ -346,11 +346,23 @@ __device__ __forceinline__ uint32_t f4_absmax_bits(const uint4 &v, uint32_t m) {
 
 // Term scales from the row's max |x| (bf16 magnitude bits; >= 0x7F80 is inf
 // or NaN, and the token's outputs become NaN): s_0 = max|x| / (6 * 2^8),
-// s_j = s_{j-1} / 6 (zero for an all-zero row).
-__device__ __forceinline__ void f4_term_scales(uint32_t m, float (&sc)[kF4Terms]) {
-    sc[0] = m < 0x7F80u ? __fdiv_rn(__uint_as_float(m << 16), 6.0f * kF4BlockHeadroom) : __int_as_float(0x7FC00000);
+// s_j = s_{j-1} / 6 (zero for an all-zero row); with them the reciprocals the
+// expansion multiplies by, inv_j = (1 / s_0) 6^j (6^j is exact in fp32; inv_j
+// is 1 / s_j to within a few ulp, which only moves the rare tie between two
+// codes -- the residual is always taken with the exact s_j), and inv6 =
+// (1 / s_0) / 6 for the block exponents.  Computed once per token.
+struct F4TokenScales {
+    float sc[kF4Terms], inv[kF4Terms], inv6;
+};
+__device__ __forceinline__ void f4_token_scales(uint32_t m, F4TokenScales &t) {
+    t.sc[0] = m < 0x7F80u ? __fdiv_rn(__uint_as_float(m << 16), 6.0f * kF4BlockHeadroom) : __int_as_float(0x7FC00000);
 #pragma unroll
-    for (int j = 1; j < kF4Terms; ++j) sc[j] = __fdiv_rn(sc[j - 1], 6.0f);
+    for (int j = 1; j < kF4Terms; ++j) t.sc[j] = __fdiv_rn(t.sc[j - 1], 6.0f);
+    const float inv0 = t.sc[0] > 0.f ? __frcp_rn(t.sc[0]) : 0.f;
+    float p6 = 1.0f;
+#pragma unroll
+    for (int j = 0; j < kF4Terms; ++j, p6 *= 6.0f) t.inv[j] = inv0 * p6;
+    t.inv6 = inv0 * (1.0f / 6.0f);
 }
 
 // Eight consecutive activations (this lane) of a 16-element block whose other
@@ -361,7 +373,7 @@ __device__ __forceinline__ void f4_term_scales(uint32_t m, float (&sc)[kF4Terms]
 // .. 2^8; rounding in the ratio can only pick the neighbouring power: a first
 // code clamped at 6 (the later terms take the excess) or one bit of the first
 // term unused.
-__device__ __forceinline__ int f4_expand8(const uint4 &raw, const float (&sc)[kF4Terms], bool finite,
+__device__ __forceinline__ int f4_expand8(const uint4 &raw, const F4TokenScales &ts, bool finite,
                                           uint32_t (&codes)[kF4Terms]) {
     float r[8];
     {
@@ -377,20 +389,20 @@ __device__ __forceinline__ int f4_expand8(const uint4 &raw, const float (&sc)[kF
     for (int i = 0; i < 8; ++i) bmax = fmaxf(bmax, fabsf(r[i]));
     bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
     int e = -9;
-    if (finite && sc[0] > 0.f) {
-        const float ratio = __fdiv_rn(bmax, 6.0f * sc[0]);
+    if (finite && ts.sc[0] > 0.f) {
+        const float ratio = bmax * ts.inv6;
         const uint32_t u = __float_as_uint(ratio);
-        const int E = (int)(u >> 23) - 127;  // ratio >= 0; 0 or subnormal give E = -127
+        const int E = (int)(u >> 23) - 127;  // ratio >= 0 and finite here; 0 or subnormal give E = -127
         if (ratio > 0.f) e = E + ((u & 0x7FFFFFu) != 0u ? 1 : 0);
         e = min(max(e, -9), 8);
     }
-    const float b = __int_as_float((e + 127) << 23);  // 2^e
+    const float b = __int_as_float((e + 127) << 23), binv = __int_as_float((127 - e) << 23);  // 2^e, 2^-e
 #pragma unroll
     for (int j = 0; j < kF4Terms; ++j) {
         codes[j] = 0;
-        const float sj = sc[j] * b;  // exact: a power-of-two multiple
+        const float sj = ts.sc[j] * b;  // exact: a power-of-two multiple
         if (finite && sj >= 1.17549435e-38f) {  // a subnormal scale's term is below any output's rounding
-            const float inv = __frcp_rn(sj);
+            const float inv = ts.sc[j] >= 1.17549435e-38f ? ts.inv[j] * binv : __frcp_rn(sj);
             float q[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) q[i] = r[i] * inv;
@@ -450,17 +462,19 @@ __global__ void __maxnreg__(64) fp4_xprep_kernel(const uint16_t *__restrict__ x,
 #pragma unroll
     for (int w = 0; w < kF4XprepThreads / 32; ++w) m = max(m, wmax[w]);
     const bool finite = m < 0x7F80u;
-    float sc[kF4Terms];
-    f4_term_scales(m, sc);
-    if (blockIdx.x == 0 && tid < kF4Terms) {
+    __shared__ F4TokenScales tok;  // the token's scales, computed once
+    if (tid == 0) {
+        f4_token_scales(m, tok);
+        if (blockIdx.x == 0) {
 #pragma unroll
-        for (int j = 0; j < kF4Terms; ++j)
-            if (tid == j) xs[t * kF4Terms + j] = sc[j];
+            for (int j = 0; j < kF4Terms; ++j) xs[t * kF4Terms + j] = tok.sc[j];
+        }
     }
+    __syncthreads();
     const int k0 = own * 8;
     if (k0 >= K) return;  // whole warps: K / 8 is a multiple of 32
     uint32_t codes[kF4Terms];
-    const int e = f4_expand8(mine, sc, finite, codes);
+    const int e = f4_expand8(mine, tok, finite, codes);
     const int kc = k0 >> 8;
     uint8_t *const tile = xq + (size_t)kc * f4_slot_bytes(cols);
 #pragma unroll

@@ -133,7 +133,7 @@ def test_mid_m_swiglu():
 
 
 def test_mid_m_caller_workspace_and_fallback():
-    N, K, n = 2048, 2048, 32
+    N, K, n = 2048, 4096, 32
     packed, scale, g, x = make_case(N, K, n, 2, 3)
     y64, _ = oracle.gemv(packed, scale, g, x)
     wp, ws, gs, xt = to_gpu(packed, scale, g, x)
