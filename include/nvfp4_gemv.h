@@ -63,7 +63,7 @@ typedef enum nvfp4_variant {
     NVFP4_VARIANT_TC = 4,       /* TMA ring + dequant into tensor memory + tcgen05.mma kind::f16 */
     NVFP4_VARIANT_FP4 = 5       /* TMA ring straight into block-scaled tcgen05.mma kind::mxf4nvf4 (W as
                                    stored, X as a sum of 8 NVFP4 terms written by a small prep kernel);
-                                   AUTO's choice for n <= 16 */
+                                   AUTO's choice for K <= 32768 */
 } nvfp4_variant;
 
 /* Token tiling.  ONE_PASS streams W once for all n tokens (chunks of up to 16
@@ -83,9 +83,9 @@ typedef struct nvfp4_gemv_opts {
     int stages;              /* 0 = as many TMA ring stages as shared memory allows; else 2..8 */
     void *workspace;         /* NULL = library-owned per-stream workspace; else device memory */
     size_t workspace_bytes;  /* size of `workspace` (see nvfp4_gemv_workspace_size); if nonzero (with or without
-                                `workspace`) the plan keeps its scratch within it: when AUTO's first choice
-                                needs more, the other fast kernel is tried (for n > 16: the FP4 kernel in
-                                16-token passes), then the tcgen05 kernel in 8-token passes */
+                                `workspace`) the plan keeps its scratch within it: when the FP4 plan needs
+                                more, AUTO takes the tcgen05 kernel, in 8-token passes if its 32-token pass
+                                needs more too */
     int inflight;            /* FP4 kernel: most weight stages requested and not yet landed per CTA (0 = default) */
 } nvfp4_gemv_opts;
 
@@ -108,19 +108,18 @@ typedef struct nvfp4_gemv_plan_info {
  * y_bf16: device, written.  n >= 0 (n == 0 is a no-op), N >= 1, K >= 16 and
  * K % 16 == 0.  Any n is accepted.  The fast paths need K % 256 == 0 and
  * 16-byte aligned w_packed, w_scale_e4m3 and x_bf16 (other inputs take the
- * GENERIC kernel).  For n <= 16 and K <= 32768 AUTO takes the FP4 kernel: one
- * read of W for all n tokens, each token's activations written as 8 NVFP4
- * terms (every 16-element block with its own power-of-two scale, so the full
- * bf16 range is taken; a block's terms leave at most 1.5e-7 of its largest
- * entry) by a small prep kernel launched ahead of the GEMV.  Above 16 tokens
- * (or K > 32768) it takes the tcgen05 f16 kernel: one read of W per 32 tokens
- * (X converted by one extra small kernel per pass), the weights of a pass that
- * another follows being left in L2.  Within one kernel every output equals the
- * single-token call's bit for bit, whatever n; since AUTO's kernel depends on
- * n, calls of different n agree to the parity tolerance, and bit for bit when
- * both take the same kernel (n <= 16: FP4).  The streaming CUDA-core kernels
- * (MMA, SIMT) take up to 16 tokens per pass (fewer when n * K is too large for
- * shared memory), each pass re-reading W.
+ * GENERIC kernel).  For K <= 32768 AUTO takes the FP4 kernel: one read of W
+ * for up to 16 tokens (passes of 16 above, the weights of a pass that another
+ * follows kept in L2), each token's activations written as 8 NVFP4 terms
+ * (every 16-element block with its own power-of-two scale, so the full bf16
+ * range is taken; a block's terms leave at most 1.5e-7 of its largest entry)
+ * by a small prep kernel launched ahead of the GEMV.  Every output equals the
+ * single-token call's bit for bit, whatever n.  For K > 32768 it takes the
+ * tcgen05 f16 kernel (one read of W per 8 tokens, or per 32 with X converted
+ * by one extra small kernel per pass; on request also for smaller K, where it
+ * showed rare run-to-run differences with long unit ranges per CTA on GB300).
+ * The streaming CUDA-core kernels (MMA, SIMT) take up to 16 tokens per pass
+ * (fewer when n * K is too large for shared memory), each pass re-reading W.
  * The tcgen05 path scales X by 2^-8 before its f16 conversion: entries with
  * |x| >= 65520 * 2^8 (about 1.68e7) are out of its range and set the device
  * error word (nvfp4_device_error), and entries below 2^-6 lose relative
@@ -198,7 +197,7 @@ nvfp4_status nvfp4_gemv_batched_noalloc(const uint8_t *w_packed, const uint8_t *
  * e.g. with nvfp4_quantize_bf16).  x_bf16 [n][K]; h_bf16 [n][F] is written.
  * Same conventions and errors as nvfp4_gemv_batched (same invariant: a batched
  * call equals n single-token calls bit for bit); runs on the tensor-core
- * paths only (FP4 for n <= 16, tcgen05 above), so K % 256 != 0 or unaligned
+ * paths only (FP4, or tcgen05 for K > 32768), so K % 256 != 0 or unaligned
  * inputs give NVFP4_ERR_UNSUPPORTED.
  * F >= 1.
  */

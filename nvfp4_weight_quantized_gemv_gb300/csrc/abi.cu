@@ -367,18 +367,20 @@ static std::vector<int> greedy_321(int n) {
     return t;
 }
 
-// AUTO's choice of kernel for a fast-path call: FP4 for n <= 16 and the
-// tcgen05 kernel above (default), the tcgen05 kernel only, or FP4 in passes of
-// 16 tokens for any n.
-enum AutoMode { kAutoDefault = 0, kAutoTcOnly = 1, kAutoFp4Passes = 2 };
+// AUTO's choice of kernel for a fast-path call: the FP4 kernel (passes of
+// up to 16 tokens) when K allows it (default), or the tcgen05 kernel only.
+enum AutoMode { kAutoDefault = 0, kAutoTcOnly = 1 };
 static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nvfp4_gemv_opts &o, int sms,
                                      int smem_optin, int tc_per_pass, AutoMode mode, Plan *plan);
 
-// AUTO picks the FP4 kernel for n <= 16 (one pass of W for every token) and
-// the tcgen05 kernel with 32 staged tokens above.  When the caller declares a
-// scratch size (workspace_bytes) too small for that plan, AUTO tries the other
-// of the two (the FP4 kernel in 16-token passes for n > 16), then the
-// tcgen05 kernel in 8-token passes.
+// AUTO picks the FP4 kernel, in passes of up to 16 tokens (one read of W for
+// n <= 16; the weights of a pass that another follows are kept in L2), for
+// K <= 32768, and the tcgen05 f16 kernel above that.  The tcgen05 kernel's
+// 32-token mode is not AUTO's choice for n > 16: on GB300 it showed rare
+// run-to-run differences with long unit ranges per CTA whose cause is not
+// found.  When the caller declares a scratch size (workspace_bytes) too
+// small for the FP4 plan, AUTO takes the tcgen05 kernel, in 8-token passes if
+// its 32-token pass does not fit either.
 static nvfp4_status make_plan_uncached(int n, int N, int K, bool fast_ok, const nvfp4_gemv_opts &o, int sms,
                                        int smem_optin, Plan *plan);
 
@@ -420,12 +422,8 @@ static nvfp4_status make_plan_uncached(int n, int N, int K, bool fast_ok, const 
     auto too_big = [&](const Plan *pl) { return small_ws && o.workspace_bytes < pl->ws_bytes; };
     nvfp4_status st =
         make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kTcMaxTokensPerPass, kAutoDefault, plan);
-    if (st == NVFP4_OK && o.variant == kAuto && too_big(plan)) {
-        if (plan->variant == kFp4)
-            st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kTcMaxTokensPerPass, kAutoTcOnly, plan);
-        else if (plan->variant == kTc && K <= kF4MaxK)
-            st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kTcMaxTokensPerPass, kAutoFp4Passes, plan);
-    }
+    if (st == NVFP4_OK && o.variant == kAuto && too_big(plan) && plan->variant == kFp4)
+        st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, kTcMaxTokensPerPass, kAutoTcOnly, plan);
     if (st == NVFP4_OK && plan->variant == kTc && plan->tc_tokens == 32 && too_big(plan))
         st = make_plan_tokens(n, N, K, fast_ok, o, sms, smem_optin, 8, kAutoTcOnly, plan);
     return st;
@@ -437,8 +435,7 @@ static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nv
     p.variant = o.variant;
     const bool tc_ok = fast_ok;
     if (p.variant == kAuto) {
-        const bool fp4_ok = fast_ok && K <= kF4MaxK &&
-                            (mode == kAutoFp4Passes || (mode == kAutoDefault && n <= kF4MaxTokensPerPass));
+        const bool fp4_ok = fast_ok && K <= kF4MaxK && mode != kAutoTcOnly;
         p.variant = fp4_ok ? kFp4 : tc_ok ? kTc : kGeneric;
     }
     if ((p.variant == kMma || p.variant == kSimt) && !fast_ok)

@@ -72,7 +72,7 @@ extern "C" nvfp4_status nvfp4_gemv_batched_noalloc(const uint8_t *w_packed, cons
     if (dev < 0 || dev >= kMaxDevices)
         return noalloc_fail(NVFP4_ERR_UNSUPPORTED, "nvfp4_gemv_batched_noalloc: device ordinal too large");
     size_t counter_bytes = 0, needed = 0;
-    nvfp4_gemv_opts cap;  // plan within the static scratch (32-token passes fall back to 16 if it is too small)
+    nvfp4_gemv_opts cap;  // plan within the static scratch (AUTO falls back to a smaller plan if it is too small)
     std::memset(&cap, 0, sizeof cap);
     cap.workspace_bytes = kNoAllocScratchBytes;
     // Inputs off 16-byte alignment (or K % 256 != 0) take the generic kernel,

@@ -136,16 +136,18 @@ def test_one_pass_plan():
     if tc8 < f4:
         assert nv.nvfp4_gemv_plan(8, 14336, 5120, workspace_bytes=tc8)["variant"] == "tc"
     assert nv.nvfp4_gemv_plan(8, 14336, 5120, workspace_bytes=f4)["variant"] == "fp4"
-    # more than 16 tokens: one pass of up to 32 (X streamed per unit), then more
-    assert nv.nvfp4_gemv_plan(20, 4096, 4096)["tile_tokens"] == [20]
-    assert nv.nvfp4_gemv_plan(32, 14336, 5120)["tile_tokens"] == [32]
-    assert nv.nvfp4_gemv_plan(64, 14336, 5120)["tile_tokens"] == [32, 32]
-    assert nv.nvfp4_gemv_plan(40, 14336, 5120)["tile_tokens"] == [32, 8]
-    # a declared scratch size too small for the 32-token pass: FP4 16-token passes
-    small = nv.nvfp4_gemv_workspace_size(16, 14336, 5120)
-    assert nv.nvfp4_gemv_workspace_size(32, 14336, 5120) > small
-    capped = nv.nvfp4_gemv_plan(40, 14336, 5120, workspace_bytes=small)
-    assert capped["tile_tokens"] == [16, 16, 8] and capped["variant"] == "fp4"
+    # more than 16 tokens: FP4 passes of 16 (the tcgen05 kernel's 32-token mode on request)
+    assert nv.nvfp4_gemv_plan(20, 4096, 4096)["tile_tokens"] == [16, 4]
+    assert nv.nvfp4_gemv_plan(40, 14336, 5120)["tile_tokens"] == [16, 16, 8]
+    assert nv.nvfp4_gemv_plan(40, 14336, 5120)["variant"] == "fp4"
+    assert nv.nvfp4_gemv_plan(32, 14336, 5120, variant=nv.VARIANT_TC)["tile_tokens"] == [32]
+    assert nv.nvfp4_gemv_plan(64, 14336, 5120, variant=nv.VARIANT_TC)["tile_tokens"] == [32, 32]
+    assert nv.nvfp4_gemv_plan(40, 14336, 5120, variant=nv.VARIANT_TC)["tile_tokens"] == [32, 8]
+    # an explicit tcgen05 call with a scratch size too small for its 32-token pass: 8-token passes
+    tc8s = nv.nvfp4_gemv_workspace_size(8, 14336, 5120, variant=nv.VARIANT_TC)
+    assert nv.nvfp4_gemv_workspace_size(32, 14336, 5120, variant=nv.VARIANT_TC) > tc8s
+    assert nv.nvfp4_gemv_plan(20, 14336, 5120, variant=nv.VARIANT_TC,
+                              workspace_bytes=tc8s)["tile_tokens"] == [8, 8, 4]
     # beyond the FP4 kernel's K: the tcgen05 kernel's 8-token passes
     tc8 = nv.nvfp4_gemv_workspace_size(8, 1024, 33024)
     assert nv.nvfp4_gemv_plan(20, 1024, 33024, workspace_bytes=tc8)["tile_tokens"] == [8, 8, 4]

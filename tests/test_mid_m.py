@@ -1,14 +1,14 @@
-"""GPU parity of the mid-M path (n = 17..64 tokens): the tcgen05 kernel with 32
-staged tokens, X converted once to f16 x 2^-8 and streamed per unit through a
-ring, up to 32 tokens per read of W (the widths atlas #266 serves with its
-mid-M tile GEMM: verify and prefill batches).
+"""GPU parity of the mid-M widths (n = 17..64 tokens, the widths atlas #266
+serves with its mid-M tile GEMM: verify and prefill batches): AUTO's FP4
+kernel in passes of 16 tokens (the weights of a pass that another follows
+kept in L2), and the tcgen05 kernel's 32-token mode (X converted once to f16
+x 2^-8 and streamed per unit through a ring, 32 tokens per read of W).
 
 Tolerance as for the GEMV: |y_gpu - y_ref| <= 1e-2 * (|y_ref| + 1), y_ref the
-oracle's unrounded fp64 value.  The k-group partition is the one of n <= 16,
-so a batched call still equals the single-token calls of the same kernel bit
-for bit (atlas #266, "Correctness argument"; AUTO takes the FP4 kernel for
-n <= 16, so the single-token calls here name the tcgen05 variant).  Inputs: oracle-quantized W ~ N(0, 0.02), X ~ N(0, 1)
-bf16 (synth.py).
+oracle's unrounded fp64 value.  Each kernel's partition does not depend on n,
+so a batched call equals the single-token calls of the same kernel bit for bit
+(atlas #266, "Correctness argument").  Inputs: oracle-quantized W ~ N(0, 0.02),
+X ~ N(0, 1) bf16 (synth.py).
 """
 from __future__ import annotations
 
@@ -60,21 +60,23 @@ def assert_close(y16, y64):
     assert not bad.any(), f"{bad.sum()} of {bad.size} out of tolerance; worst {err.max()}"
 
 
-@pytest.mark.parametrize("N,K,n,tiles", [
-    (1000, 1024, 17, [17]),        # one 32-token pass, 15 zero-filled token rows
-    (384, 2048, 32, [32]),         # a full pass
-    (2000, 512, 24, [24]),         # short segments (two units per row block)
-    (256, 8192, 20, [20]),         # deep K: several k-groups, many split parts
-    (700, 1280, 40, [32, 8]),      # a second pass of 8 tokens with the 32-token kernel
-    (300, 768, 64, [32, 32]),      # ragged rows, two full passes
-    (129, 256, 33, [32, 1]),       # one unit per row block, a one-token tail pass
+@pytest.mark.parametrize("variant", ["auto", "tc"])
+@pytest.mark.parametrize("N,K,n,tiles,tc_tiles", [
+    (1000, 1024, 17, [16, 1], [17]),          # a one-token second pass / one 32-token pass
+    (384, 2048, 32, [16, 16], [32]),          # two full FP4 passes / a full 32-token pass
+    (2000, 512, 24, [16, 8], [24]),           # short segments (two units per row block)
+    (256, 8192, 20, [16, 4], [20]),           # deep K
+    (700, 1280, 40, [16, 16, 8], [32, 8]),    # three passes / a second pass of 8 tokens
+    (300, 768, 64, [16, 16, 16, 16], [32, 32]),
+    (129, 256, 33, [16, 16, 1], [32, 1]),     # one unit per row block, a one-token tail pass
 ])
-def test_mid_m_full_output(N, K, n, tiles):
-    assert nv.nvfp4_gemv_plan(n, N, K)["tile_tokens"] == tiles
+def test_mid_m_full_output(variant, N, K, n, tiles, tc_tiles):
+    v = nv.VARIANT_TC if variant == "tc" else 0
+    assert nv.nvfp4_gemv_plan(n, N, K, variant=v)["tile_tokens"] == (tc_tiles if variant == "tc" else tiles)
     packed, scale, g, x = make_case(N, K, n, 3, 4, outlier=0.01)
     y64, _ = oracle.gemv(packed, scale, g, x)
     wp, ws, gs, xt = to_gpu(packed, scale, g, x)
-    assert_close(bits(nv.nvfp4_gemv_batched(wp, ws, gs, xt)), y64)
+    assert_close(bits(nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt, variant=v)), y64)
 
 
 @pytest.mark.parametrize("n", [32, 40])
@@ -82,12 +84,11 @@ def test_mid_m_equals_single_token_calls(n):
     N, K = 1536, 2048
     packed, scale, g, x = make_case(N, K, n, 5, 6)
     wp, ws, gs, xt = to_gpu(packed, scale, g, x)
-    full = bits(nv.nvfp4_gemv_batched(wp, ws, gs, xt))
-    assert nv.nvfp4_gemv_plan(n, N, K)["variant"] == "tc"
-    for t in range(n):
-        # the same kernel for one token (AUTO would take the FP4 kernel at n = 1)
-        one = bits(nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt[t:t + 1].contiguous(), variant=nv.VARIANT_TC))
-        assert np.array_equal(one[0], full[t]), t
+    for v in (0, nv.VARIANT_TC):  # AUTO (FP4 passes) and the tcgen05 32-token mode
+        full = bits(nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt, variant=v))
+        for t in range(n):
+            one = bits(nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt[t:t + 1].contiguous(), variant=v))
+            assert np.array_equal(one[0], full[t]), (v, t)
 
 
 @pytest.mark.parametrize("n", [32, 64])
@@ -103,7 +104,7 @@ def test_mid_m_full_size_qkv_sampled(n):
     ref64, _ = oracle.gemv_points(packed, scale, g, x, toks, rows)
     assert_close(y16[toks, rows], ref64)
     for t in (0, 17, n - 1):  # batched == single token on the full-size launch configuration
-        one = bits(nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt[t:t + 1].contiguous(), variant=nv.VARIANT_TC))
+        one = bits(nv.nvfp4_gemv_batched(wp, ws, gs, xt[t:t + 1].contiguous()))
         assert np.array_equal(one[0], y16[t]), t
 
 
@@ -133,18 +134,19 @@ def test_mid_m_swiglu():
 
 
 def test_mid_m_caller_workspace_and_fallback():
-    N, K, n = 2048, 4096, 32
+    N, K, n = 2048, 2048, 32
     packed, scale, g, x = make_case(N, K, n, 2, 3)
     y64, _ = oracle.gemv(packed, scale, g, x)
     wp, ws, gs, xt = to_gpu(packed, scale, g, x)
     big = torch.zeros(nv.nvfp4_gemv_workspace_size(n, N, K), dtype=torch.uint8, device="cuda")
     y_big = bits(nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt, workspace=big))
     assert_close(y_big, y64)
-    # a scratch sized for 16 tokens of the FP4 kernel: the call takes its
-    # 16-token passes instead (another kernel: within the tolerance)
-    small_bytes = nv.nvfp4_gemv_workspace_size(16, N, K)
+    # a scratch too small for the FP4 plan but enough for the tcgen05 kernel's
+    # 8-token passes: the call takes those (another kernel: within the tolerance)
+    small_bytes = nv.nvfp4_gemv_workspace_size(8, N, K, variant=nv.VARIANT_TC)
     assert small_bytes < big.numel()
-    assert nv.nvfp4_gemv_plan(n, N, K, workspace_bytes=small_bytes)["variant"] == "fp4"
+    plan = nv.nvfp4_gemv_plan(n, N, K, workspace_bytes=small_bytes)
+    assert plan["variant"] == "tc" and plan["tile_tokens"] == [8, 8, 8, 8]
     small = torch.zeros(small_bytes, dtype=torch.uint8, device="cuda")
     assert_close(bits(nv.nvfp4_gemv_batched_ex(wp, ws, gs, xt, workspace=small)), y64)
     y = torch.empty((n, N), dtype=torch.bfloat16, device="cuda")

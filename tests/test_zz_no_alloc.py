@@ -7,9 +7,9 @@ receive pointers from a host program owning the memory.  For them the library
 keeps the kernel's scratch in a static device array.  These tests call that
 entry point through the C ABI (ctypes): twice in a row against the ordinary
 entry point (same plan, so bit for bit) and sampled points of the oracle
-within the parity tolerance; a call whose 32-token pass does not fit the
-scratch (two 16-token FP4 passes, as the _ex entry point with an 8 MiB
-workspace); and a call refused because no plan fits.  It lives in its own file, collected last, and needs no state
+within the parity tolerance; a deep-K call of 32 tokens (two 16-token FP4
+passes, as the _ex entry point with an 8 MiB workspace); and a call refused
+because no plan fits.  It lives in its own file, collected last, and needs no state
 from earlier tests.
 """
 from __future__ import annotations
@@ -78,16 +78,15 @@ def _check_sampled(wp, ws, gs, xt, y, seed):
     assert np.all(np.abs(got - ref) <= TOL * (np.abs(ref) + 1.0))
 
 
-def test_noalloc_takes_16_token_passes_when_32_do_not_fit():
-    """n = 32 at K = 16384: the tcgen05 kernel's 32-token pass needs more than
-    the 8 MiB static scratch, so the call runs two 16-token passes of the FP4
-    kernel -- the plan, and the bits, of the _ex entry point given an 8 MiB
-    workspace."""
+def test_noalloc_two_passes_at_deep_k():
+    """n = 32 at K = 16384: AUTO's plan is two 16-token FP4 passes, within the
+    8 MiB static scratch -- the plan, and the bits, of the _ex entry point
+    given an 8 MiB workspace."""
     nv.build()
     oracle.build()
     N, K, n = 14336, 16384, 32
     cap = 8 << 20
-    assert nv.nvfp4_gemv_workspace_size(n, N, K) > cap
+    assert nv.nvfp4_gemv_workspace_size(n, N, K) <= cap
     plan = nv.nvfp4_gemv_plan(n, N, K, workspace_bytes=cap)
     assert plan["tile_tokens"] == [16, 16] and plan["variant"] == "fp4"
     wp, ws, gs, xt = _case(N, K, n, 40, 41)
