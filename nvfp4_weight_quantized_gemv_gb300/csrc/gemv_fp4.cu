@@ -447,9 +447,9 @@ __global__ void __maxnreg__(64) fp4_xprep_kernel(const uint16_t *__restrict__ x,
 #pragma unroll
     for (int j = 0; j < L; ++j) {
         const int i = tid + j * kF4XprepThreads;
-        v[j] = i < nvec ? __ldg(xr + i) : make_uint4(0, 0, 0, 0);
+        v[j] = i < nvec ? ld_dep_v4(xr + i) : make_uint4(0, 0, 0, 0);
     }
-    const uint4 mine = own < nvec ? __ldg(xr + own) : make_uint4(0, 0, 0, 0);  // one of the above: same request
+    const uint4 mine = own < nvec ? ld_dep_v4(xr + own) : make_uint4(0, 0, 0, 0);  // one of the above: same line
     uint32_t m = 0;
 #pragma unroll
     for (int j = 0; j < L; ++j) m = f4_absmax_bits(v[j], m);
@@ -865,9 +865,9 @@ __global__ void __maxnreg__(128)
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
         const int r = 32 * q + lane;
         griddep_wait();  // the term scales, g, the workspace and Y belong to this call from here on
-        const float g = __ldg(p.gscale);
+        const float g = ld_dep_f32(p.gscale);
         for (int i = (int)threadIdx.x - kF4WarpEpi0 * 32; i < 16 * kF4Terms; i += 128)
-            tscale[i] = i < p.n * kF4Terms ? __ldcg(p.xs + i) : 0.f;
+            tscale[i] = i < p.n * kF4Terms ? ld_dep_f32(p.xs + i) : 0.f;
         named_sync(1, 128);
         // the other part of a two-part row block, loaded ahead of time
         float pre_part[16];

@@ -618,7 +618,7 @@ __global__ void __maxnreg__(kTcMaxRegs)
         zero_x_pad(warp - kTcWarpEpilogue0);
         griddep_wait();  // X, the global scale, the workspace and Y belong to this call from here on
         if (!convert_x(warp - kTcWarpEpilogue0) && lane == 0) atomicOr(p.err, kDevErrTimeoutFull);
-        const float gs = __ldg(p.gscale) * kTcXUnscale;
+        const float gs = ld_dep_f32(p.gscale) * kTcXUnscale;
         (void)KC;
         int seg = 0, kl = kl0, rb = rb0;
         for (int i = 0; i < count; ++seg) {
@@ -762,7 +762,7 @@ __device__ __forceinline__ void tc_reduce_sweep(const StreamParams &p, const TcP
             }
         }
     }
-    tc_store_row(p, acc, row, __ldg(p.gscale) * kTcXUnscale, h * TT);
+    tc_store_row(p, acc, row, ld_dep_f32(p.gscale) * kTcXUnscale, h * TT);
 }
 
 template <int T>
@@ -800,7 +800,7 @@ __global__ void __launch_bounds__(256) tc_x16_kernel(const uint16_t *__restrict_
     griddep_launch_dependents();
     uint32_t bad = 0;
     for (long long c = (long long)blockIdx.x * 256 + threadIdx.x; c < chunks; c += (long long)gridDim.x * 256) {
-        uint4 v = __ldg(reinterpret_cast<const uint4 *>(x) + c);
+        uint4 v = ld_dep_v4(reinterpret_cast<const uint4 *>(x) + c);
         v.x = bf16x2_to_f16x2_scaled(v.x, bad);
         v.y = bf16x2_to_f16x2_scaled(v.y, bad);
         v.z = bf16x2_to_f16x2_scaled(v.z, bad);

@@ -23,6 +23,27 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 // Programmatic dependent launch: wait for the grid ahead on the stream to
 // finish (and its writes to be visible) / let the next grid start launching.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Loads of data that the grid ahead may write (X, the global scale, the term
+// scales), issued after griddep_wait().  Not the read-only path
+// (ld.global.nc, __ldg): its loads presume data constant for the whole life
+// of the kernel, and a kernel launched early under programmatic dependent
+// launch starts before its input is final -- on GB300 such a load returned
+// the value from before the grid ahead wrote it.  These are L2-coherent and
+// kept after the wait by the clobber.
+__device__ __forceinline__ uint4 ld_dep_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ float ld_dep_f32(const float *p) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

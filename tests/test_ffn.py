@@ -96,6 +96,29 @@ def test_ffn_swiglu_matches_oracle(n):
     assert nv.nvfp4_device_error() == 0
 
 
+@pytest.mark.parametrize("n,variant", [(1, "auto"), (3, "auto"), (4, "auto"), (8, "auto"), (4, "tc"), (24, "tc")])
+def test_down_projection_reads_h_written_by_the_kernel_ahead(n, variant):
+    """The down projection launches before the gate/up kernel ahead of it has
+    finished (programmatic dependent launch) and must read h only as that
+    kernel left it: h starts as NaN, so any read of it from before shows."""
+    D, F = 1024, 2048
+    gu = dev_weights(*joint_gate_up(F, D, seed=21))
+    down = dev_weights(*oracle.quantize(synth.weights_f32(D, F, 23)))
+    x = dev_x(synth.activations_bf16(n, D, seed=24))
+    v = nv.VARIANT_TC if variant == "tc" else nv.VARIANT_AUTO
+    h = torch.empty((n, F), dtype=torch.bfloat16, device="cuda")
+    nv.nvfp4_gemv_swiglu(*gu, x, h=h)
+    torch.cuda.synchronize()
+    y_ref = host_bits(nv.nvfp4_gemv_batched_ex(*down, h, variant=v))  # h final before the launch
+    for _ in range(3):
+        h2 = torch.full((n, F), float("nan"), dtype=torch.bfloat16, device="cuda")
+        nv.nvfp4_gemv_swiglu(*gu, x, h=h2)
+        y = host_bits(nv.nvfp4_gemv_batched_ex(*down, h2, variant=v))
+        assert np.array_equal(host_bits(h2), host_bits(h))
+        assert np.array_equal(y, y_ref)
+    assert nv.nvfp4_device_error() == 0
+
+
 def test_gemv_swiglu_needs_the_tcgen05_path():
     packed, scale, g = joint_gate_up(32, 784, seed=5)   # K % 256 != 0
     x = synth.activations_bf16(2, 784, seed=6)
