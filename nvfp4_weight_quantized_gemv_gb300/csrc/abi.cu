@@ -233,6 +233,7 @@ struct Plan {
     // and the workspace regions after the partial tiles
     int f4_cols_max = 0, f4_max_seg = 0, f4_max_parts = 0, f4_inflight = 0;
     bool f4_x_resident = false;
+    int f4_cluster = 0;  // CTAs per row block when the grid splits every row block evenly (summed in a cluster)
     size_t f4_xq_offset = 0, f4_xt_offset = 0, f4_et_offset = 0;
 };
 
@@ -476,6 +477,13 @@ static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nv
         nvfp4_status st = f4_partition(N, K, ctas, &p.f4_max_seg, &p.f4_max_parts);
         if (st != NVFP4_OK) return st;
         p.f4_cols_max = f4_cols(max_tile);
+        {
+            // RB p CTAs with KC % p == 0: every CTA holds 1 / p of one row block;
+            // the p parts of a row block are consecutive CTAs, one cluster
+            const int RBc = (N + kUnitRows - 1) / kUnitRows, KCc = K / kTcUnitKHost;
+            const int parts = ctas % RBc == 0 ? ctas / RBc : 0;
+            p.f4_cluster = (parts >= 2 && parts <= 8 && KCc % parts == 0) ? parts : 0;
+        }
         // leave room on the SM for one X-prep CTA of the next call beside the GEMV
         const int limit = smem_optin - 4096;
         const int KC = K / kTcUnitKHost;
@@ -654,6 +662,7 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
         fp.swiglu = swiglu ? 1 : 0;
         fp.inflight = plan.f4_inflight;
         fp.x_resident = plan.f4_x_resident ? 1 : 0;
+        fp.cluster = plan.f4_cluster;
         const size_t y_stride_f4 = swiglu ? (size_t)N / 2 : (size_t)N;
         int t0 = 0;
         for (int tn : plan.tiles) {

@@ -193,7 +193,13 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, unsigned parity) {
 // One row's outputs for all n tokens (v[t] = token t's sum of terms, before
 // g): y = bf16(v g), or with swiglu the gated form of rows 2f / 2f + 1 held by
 // lanes 2i / 2i + 1 (every lane of the warp must call it).
-__device__ __forceinline__ void f4_store_row(const F4Params &p, const float (&v)[16], int row, float g) {
+// The output side of the parameters (F4Params, or F4Out by value).
+struct F4Out {
+    uint16_t *y;
+    int N, n, swiglu;
+};
+template <typename P>
+__device__ __forceinline__ void f4_store_row(const P &p, const float (&v)[16], int row, float g) {
     const int lane = threadIdx.x & 31;
     if (!p.swiglu) {
         if (row < p.N) {
@@ -287,6 +293,56 @@ __device__ __forceinline__ void f4_sum_parts(const F4Params &p, float (&sum)[16]
     }
 #pragma unroll
     for (int t = 4 * KQ; t < 16; ++t) sum[t] = 0.f;
+}
+
+// Sum of the `cl` parts of this thread's row held by the CTAs of its cluster
+// (shared-memory address `mine` in each), in rank order: the same order,
+// and so the same rounding, as the workspace path's CTA order.  The loads of
+// up to 8 / KQ parts are in flight together.
+template <int KQ>
+__device__ __forceinline__ void f4_sum_cluster(float (&sum)[16], uint32_t mine, int cl) {
+    constexpr int B = 8 / KQ;
+    for (int k0 = 0; k0 < cl; k0 += B) {
+        float4 f[B][KQ];
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            if (k0 + j < cl) {
+                const uint32_t src = cluster_map(mine, (uint32_t)(k0 + j));
+#pragma unroll
+                for (int qd = 0; qd < KQ; ++qd) f[j][qd] = ld_cluster_f4(src + 16 * qd);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            if (k0 + j >= cl) break;
+#pragma unroll
+            for (int qd = 0; qd < KQ; ++qd) {
+                const float4 v = f[j][qd];
+                if (k0 + j == 0) {
+                    sum[4 * qd] = v.x;
+                    sum[4 * qd + 1] = v.y;
+                    sum[4 * qd + 2] = v.z;
+                    sum[4 * qd + 3] = v.w;
+                } else {
+                    sum[4 * qd] += v.x;
+                    sum[4 * qd + 1] += v.y;
+                    sum[4 * qd + 2] += v.z;
+                    sum[4 * qd + 3] += v.w;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 4 * KQ; t < 16; ++t) sum[t] = 0.f;
+}
+
+// The cluster's sum of this thread's row, stored (out of line: it runs once
+// per CTA, and inlined it would add to the epilogue's register pressure).
+template <int KQ>
+__device__ __noinline__ void f4_cluster_finish(const F4Out p, uint32_t mine, int cl, int row, float g) {
+    float sum[16];
+    f4_sum_cluster<KQ>(sum, mine, cl);
+    f4_store_row(p, sum, row, g);
 }
 
 // Eight fp32 values -> eight E2M1 codes, value j in nibble j (the hardware
@@ -555,6 +611,12 @@ __global__ void __maxnreg__(128)
     if (sbase & 1023u) {  // the swizzled tiles need a 1024-byte aligned base; never expected
         griddep_wait();
         if (threadIdx.x == 0) atomicOr(p.err, kF4ErrSmemBase);
+        if (p.cluster) {  // every CTA of the cluster takes this path (same layout): both cluster phases
+            cluster_arrive();
+            cluster_wait();
+            cluster_arrive();
+            cluster_wait();
+        }
         return;
     }
     const int S = p.stages;
@@ -640,6 +702,20 @@ __global__ void __maxnreg__(128)
     if (threadIdx.x == 0) griddep_launch_dependents();
     // per stage kF4SfCols columns: the W scales (16), then the X block scales (16)
     const uint32_t sf_base = tbase + 2 * kIssuers * kDStride;
+
+    // Split row blocks summed in a cluster (p.cluster = p CTAs per row block,
+    // one segment each): the epilogue leaves this CTA's part in ring stage 0
+    // (free once the segment's MMAs are done); after a cluster barrier the
+    // CTA of rank k sums the rows of its epilogue warps q with q % p == k
+    // over the p parts in rank (= CTA) order and stores them; a second
+    // barrier keeps every CTA alive until its peers have read its part.
+    // (Measured on GB300: the hardware cluster barrier beat remote mbarrier
+    // arrivals here by ~1.2 us per call.)
+    const int cl = p.cluster;
+    const uint32_t sRed = sbase;  // [128 rows][16] fp32, a row's tokens in 64 bytes
+    bool red_pending = false;
+    int red_row = 0;
+    float g_ep = 0.f;
 
     if (warp == kF4WarpProducer) {
         // ---------------------------------------------------- weight producer
@@ -866,6 +942,7 @@ __global__ void __maxnreg__(128)
         const int r = 32 * q + lane;
         griddep_wait();  // the term scales, g, the workspace and Y belong to this call from here on
         const float g = ld_dep_f32(p.gscale);
+        g_ep = g;
         for (int i = (int)threadIdx.x - kF4WarpEpi0 * 32; i < 16 * kF4Terms; i += 128)
             tscale[i] = i < p.n * kF4Terms ? ld_dep_f32(p.xs + i) : 0.f;
         named_sync(1, 128);
@@ -886,7 +963,7 @@ __global__ void __maxnreg__(128)
             // and load it then; this CTA then adds the last part and needs no
             // count (a two-part sum is the same in either order).  The watch
             // ends when the accumulators are ready (bounded like every wait).
-            if (s == ord.nseg - 1 && !whole && cb == ca + 1) {
+            if (!cl && s == ord.nseg - 1 && !whole && cb == ca + 1) {
                 const unsigned long long t0 = globaltimer_ns();
                 for (;;) {
                     if (warp == kF4WarpEpi0 && lane == 0) {
@@ -977,6 +1054,17 @@ __global__ void __maxnreg__(128)
                 f4_store_row(p, acc, row, g);
                 continue;
             }
+            if (cl) {  // the cluster sums the parts after the loop
+#pragma unroll
+                for (int qd = 0; qd < 4; ++qd)
+                    if (4 * qd < p.n)
+                        sts128(sRed + (uint32_t)r * 64 + 16 * qd,
+                               make_uint4(__float_as_uint(acc[4 * qd]), __float_as_uint(acc[4 * qd + 1]),
+                                          __float_as_uint(acc[4 * qd + 2]), __float_as_uint(acc[4 * qd + 3])));
+                red_pending = true;
+                red_row = row;
+                continue;
+            }
             // A split row block.  This CTA adds the last part when the other
             // parts are in already -- found before the segment (and loaded
             // ahead, two-part rows) or now (loaded now) -- or when its count
@@ -1019,11 +1107,26 @@ __global__ void __maxnreg__(128)
         }
     }
 
+    if (cl) {
+        // every part of the cluster's row blocks is in its CTA's shared memory
+        // (the hardware cluster barrier: every thread of the cluster arrives,
+        // and every CTA gets here, since all its own waits are bounded)
+        cluster_arrive();
+        cluster_wait();
+        const int q = warp & 3;
+        if (warp >= kF4WarpEpi0 && warp < kF4WarpEpi0 + 4 && q % cl == (int)cluster_ctarank() && red_pending)
+            f4_cluster_finish<(NC / kF4Terms + 3) / 4>(F4Out{p.y, p.N, p.n, p.swiglu},
+                                                       sRed + (uint32_t)(32 * q + lane) * 64, cl, red_row, g_ep);
+    }
     tc::fence_before_sync();
     __syncthreads();
     if (warp == kF4WarpIssuer) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tbase, kF4TmemCols);
+    }
+    if (cl) {  // no CTA leaves while a peer may still read its part
+        cluster_arrive();
+        cluster_wait();
     }
 }
 
@@ -1045,11 +1148,72 @@ cudaError_t f4_set_smem_limit(int smem_optin) {
     return cudaSuccess;
 }
 
-cudaError_t launch_fp4(const CUtensorMap &tw, const CUtensorMap &ts, const uint16_t *x, const F4Params &p, int smem,
-                       cudaStream_t stream) {
+static const void *f4_kernel(int cols) {
+    switch (cols) {
+        case 16: return reinterpret_cast<const void *>(gemv_fp4_kernel<16>);
+        case 32: return reinterpret_cast<const void *>(gemv_fp4_kernel<32>);
+        case 48: return reinterpret_cast<const void *>(gemv_fp4_kernel<48>);
+        case 64: return reinterpret_cast<const void *>(gemv_fp4_kernel<64>);
+        case 80: return reinterpret_cast<const void *>(gemv_fp4_kernel<80>);
+        case 96: return reinterpret_cast<const void *>(gemv_fp4_kernel<96>);
+        case 112: return reinterpret_cast<const void *>(gemv_fp4_kernel<112>);
+        case 128: return reinterpret_cast<const void *>(gemv_fp4_kernel<128>);
+        default: return nullptr;
+    }
+}
+
+// Whether `ctas` CTAs in clusters of `cs` can all be resident at once (the
+// CTAs of a cluster share a GPC, so not every grid of one CTA per SM divides
+// into co-resident clusters).  Cached per (device, columns, shared memory,
+// cluster size).
+static bool f4_clusters_fit(int cols, int smem, int cs, int ctas) {
+    struct Entry {
+        int dev, cols, smem, cs, clusters;
+    };
+    static thread_local Entry cache[16];
+    static thread_local int used = 0, next = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    for (int i = 0; i < used; ++i)
+        if (cache[i].dev == dev && cache[i].cols == cols && cache[i].smem == smem && cache[i].cs == cs)
+            return cache[i].clusters * cs >= ctas;
     cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kF4Threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, f4_kernel(cols), &cfg) != cudaSuccess) {
+        cudaGetLastError();  // not fatal: the split rows go through the workspace then
+        clusters = 0;
+    }
+    cache[next] = Entry{dev, cols, smem, cs, clusters};
+    next = (next + 1) % 16;
+    if (used < 16) ++used;
+    return clusters * cs >= ctas;
+}
+
+cudaError_t launch_fp4(const CUtensorMap &tw, const CUtensorMap &ts, const uint16_t *x, const F4Params &p_in,
+                       int smem, cudaStream_t stream) {
+    F4Params p = p_in;
+    // clusters only when they can all be resident at once (one CTA per SM)
+    if (p.cluster && (p.ctas % p.cluster != 0 || !f4_clusters_fit(p.cols, smem, p.cluster, p.ctas))) p.cluster = 0;
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = p.cluster ? (unsigned)p.cluster : 1u;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t xc = {};
     xc.gridDim = dim3((unsigned)((p.K + kF4XprepElems - 1) / kF4XprepElems), (unsigned)p.n);
     xc.blockDim = dim3(kF4XprepThreads);
@@ -1070,7 +1234,7 @@ cudaError_t launch_fp4(const CUtensorMap &tw, const CUtensorMap &ts, const uint1
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.cluster ? 2 : 1;
     switch (p.cols) {
         case 16: return cudaLaunchKernelEx(&cfg, gemv_fp4_kernel<16>, tw, ts, p);
         case 32: return cudaLaunchKernelEx(&cfg, gemv_fp4_kernel<32>, tw, ts, p);

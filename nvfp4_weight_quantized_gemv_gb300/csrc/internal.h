@@ -85,6 +85,8 @@ struct F4Params {
     int ctas, row_blocks, max_seg, stages, cols, swiglu, w_keep;
     int inflight;         // weight stages requested and not yet landed, at most
     int x_resident;       // 1: all unit columns' X codes stay in shared memory; 0: streamed with each stage
+    int cluster;          // p >= 2: every row block is split over p consecutive CTAs, launched as one
+                          // cluster that sums the parts through distributed shared memory; 0: no clusters
 };
 int f4_smem_bytes(int stages, int cols, bool x_resident, int KC);
 int f4_max_stages(int cols, int smem_limit, bool x_resident, int KC);   // 0: does not fit

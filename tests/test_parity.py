@@ -170,6 +170,26 @@ def test_short_segments(variant, N, K, n, num_ctas):
     assert_close(gpu_gemv(to_gpu(packed, scale, g, x), VARIANTS[variant], num_ctas=num_ctas), y64)
 
 
+@pytest.mark.parametrize("num_ctas", [16, 24, 32, 48, 40])
+@pytest.mark.parametrize("n", [1, 5, 16])
+def test_row_blocks_split_evenly(num_ctas, n):
+    """8 row blocks of 12 units on 8 p CTAs (p = 2, 3, 4, 6): each row block's
+    p parts are summed in a cluster of p CTAs, in CTA order; 40 CTAs split
+    rows unevenly and sum through the workspace.  Parity with the oracle,
+    repeatability, and batched == single-token calls bit for bit."""
+    N, K = 1024, 3072
+    packed, scale, g, x = make_case(N, K, n, wseed=11, xseed=12)
+    dev = to_gpu(packed, scale, g, x)
+    y = gpu_gemv(dev, nv.VARIANT_FP4, num_ctas=num_ctas)
+    y64, _ = oracle.gemv(packed, scale, g, x)
+    assert_close(y, y64)
+    assert np.array_equal(gpu_gemv(dev, nv.VARIANT_FP4, num_ctas=num_ctas), y)
+    wp, ws, gs, xt = dev
+    for t in range(n):
+        yt = gpu_gemv((wp, ws, gs, xt[t:t + 1].contiguous()), nv.VARIANT_FP4, num_ctas=num_ctas)
+        assert np.array_equal(yt[0], y[t]), t
+
+
 def test_chained_calls_read_the_previous_output():
     """Back-to-back calls on one stream where call 2 reads call 1's output as X:
     the second kernel may start early (programmatic dependent launch) but must
