@@ -132,10 +132,16 @@ TRAFFIC_FILES = {
 
 
 def source_hash(names) -> str:
+    """sha256 of the named kernel sources' code: comments and blank lines
+    removed, so that a comment edit keeps the recorded counters valid."""
     csrc = os.path.join(ROOT, "nvfp4_weight_quantized_gemv_gb300", "csrc")
     h = hashlib.sha256()
     for name in names:
-        h.update(open(os.path.join(csrc, name), "rb").read())
+        text = open(os.path.join(csrc, name), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(code.encode("utf-8"))
     return h.hexdigest()
 
 

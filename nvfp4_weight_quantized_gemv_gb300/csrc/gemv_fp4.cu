@@ -36,13 +36,15 @@
 // Work split.  Units of 128 rows x 256 k (one 16 KB W tile, 128-byte swizzle,
 // plus the rows' 16 scale bytes); the persistent grid (one CTA per SM) takes
 // equal contiguous ranges of the row-block-major unit order (stream-K over all
-// of K).  A row block held whole by one CTA is finished there; the parts of a
-// split row block are written as fp32 tiles and the CTA that adds the last
-// part (an atomic count per row block, or a look at it when the others are
-// known to be in) sums them in CTA order and stores the row -- fixed order,
-// no second launch, no waiting on other CTAs.  A CTA processes the partial
-// row block at the end of its range first, so that its part is published
-// early.
+// of K).  A row block held whole by one CTA is finished there.  When the grid
+// gives every row block p equal parts, the p CTAs of a row block run as one
+// thread-block cluster and sum the parts through distributed shared memory
+// after a cluster barrier, in CTA order.  Otherwise the parts of a split row
+// block are written as fp32 tiles and the CTA that adds the last part (an
+// atomic count per row block, or a look at it when the others are known to
+// be in) sums them in CTA order and stores the row -- fixed order, no second
+// launch, no waiting on other CTAs.  A CTA processes the partial row block at
+// the end of its range first, so that its part is published early.
 //
 // Warp roles (384 threads):
 //   warp 0     weight producer: TMA of the unit's W and S tiles into a ring of S
@@ -336,10 +338,9 @@ __device__ __forceinline__ void f4_sum_cluster(float (&sum)[16], uint32_t mine, 
     for (int t = 4 * KQ; t < 16; ++t) sum[t] = 0.f;
 }
 
-// The cluster's sum of this thread's row, stored (out of line: it runs once
-// per CTA, and inlined it would add to the epilogue's register pressure).
+// The cluster's sum of this thread's row, stored.
 template <int KQ>
-__device__ __noinline__ void f4_cluster_finish(const F4Out p, uint32_t mine, int cl, int row, float g) {
+__device__ __forceinline__ void f4_cluster_finish(const F4Out p, uint32_t mine, int cl, int row, float g) {
     float sum[16];
     f4_sum_cluster<KQ>(sum, mine, cl);
     f4_store_row(p, sum, row, g);
@@ -612,6 +613,7 @@ __global__ void __maxnreg__(128)
         griddep_wait();
         if (threadIdx.x == 0) atomicOr(p.err, kF4ErrSmemBase);
         if (p.cluster) {  // every CTA of the cluster takes this path (same layout): both cluster phases
+            __syncwarp();
             cluster_arrive();
             cluster_wait();
             cluster_arrive();
@@ -1111,6 +1113,7 @@ __global__ void __maxnreg__(128)
         // every part of the cluster's row blocks is in its CTA's shared memory
         // (the hardware cluster barrier: every thread of the cluster arrives,
         // and every CTA gets here, since all its own waits are bounded)
+        __syncwarp();
         cluster_arrive();
         cluster_wait();
         const int q = warp & 3;
@@ -1125,6 +1128,7 @@ __global__ void __maxnreg__(128)
         tc::tmem_dealloc(tbase, kF4TmemCols);
     }
     if (cl) {  // no CTA leaves while a peer may still read its part
+        __syncwarp();
         cluster_arrive();
         cluster_wait();
     }
