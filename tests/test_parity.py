@@ -171,12 +171,13 @@ def test_short_segments(variant, N, K, n, num_ctas):
 
 
 @pytest.mark.parametrize("num_ctas", [16, 24, 32, 48, 40])
-@pytest.mark.parametrize("n", [1, 5, 16])
+@pytest.mark.parametrize("n", [1, 5, 16, 20])
 def test_row_blocks_split_evenly(num_ctas, n):
     """8 row blocks of 12 units on 8 p CTAs (p = 2, 3, 4, 6): each row block's
     p parts are summed in a cluster of p CTAs, in CTA order; 40 CTAs split
-    rows unevenly and sum through the workspace.  Parity with the oracle,
-    repeatability, and batched == single-token calls bit for bit."""
+    rows unevenly and sum through the workspace.  n = 20 takes two passes.
+    Parity with the oracle, repeatability, and batched == single-token calls
+    bit for bit."""
     N, K = 1024, 3072
     packed, scale, g, x = make_case(N, K, n, wseed=11, xseed=12)
     dev = to_gpu(packed, scale, g, x)
