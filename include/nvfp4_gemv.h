@@ -51,7 +51,8 @@ typedef enum nvfp4_status {
     NVFP4_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed; see nvfp4_last_error() */
     NVFP4_ERR_DEVICE_TIMEOUT = 5,  /* a kernel gave up waiting on a barrier (see nvfp4_device_error) */
     NVFP4_ERR_WORKSPACE = 6,       /* caller workspace too small */
-    NVFP4_ERR_DEVICE_INPUT = 7     /* a kernel met an input it cannot use (see nvfp4_device_error) */
+    NVFP4_ERR_DEVICE_INPUT = 7,    /* a kernel met an input it cannot use (see nvfp4_device_error) */
+    NVFP4_ERR_DEVICE_BOUNDS = 8    /* debug-bounds build: a device index check failed (see nvfp4_device_error) */
 } nvfp4_status;
 
 /* Kernel variants (selectable through nvfp4_gemv_opts; AUTO picks per shape). */
@@ -319,12 +320,18 @@ nvfp4_status nvfp4_quantize_bf16(const uint16_t *w_bf16, int N, int K, uint8_t *
  *   8        a GEMV met |x| >= 65520 * 2^8 (see nvfp4_gemv_batched);
  *   16       the device quantizer met a non-finite weight;
  *   32       the grouped expert GEMV met bad routing data;
- *   64       the tcgen05 GEMV found its dynamic shared memory off a 1024-byte
- *            boundary and computed nothing (a platform fault, never expected).
+ *   64       a tcgen05 or FP4 GEMV found its dynamic shared memory off a
+ *            1024-byte boundary and computed nothing (a platform fault, never
+ *            expected);
+ *   128      (only the library built with -DNVFP4_DEBUG_BOUNDS,
+ *            libnvfp4_gemv_debug.so) a device check of a computed workspace
+ *            index (partial tile, split-row counter) failed and the access was
+ *            skipped.
  * Returns NVFP4_ERR_DEVICE_TIMEOUT when any of bits 1, 2, 4 is set (the
  * library then also re-zeroes its own workspaces so later calls start clean),
- * else NVFP4_ERR_UNSUPPORTED when bit 64 is set, else NVFP4_ERR_DEVICE_INPUT
- * when bit 8, 16 or 32 is set, else NVFP4_OK. */
+ * else NVFP4_ERR_DEVICE_BOUNDS when bit 128 is set, else NVFP4_ERR_UNSUPPORTED
+ * when bit 64 is set, else NVFP4_ERR_DEVICE_INPUT when bit 8, 16 or 32 is set,
+ * else NVFP4_OK. */
 nvfp4_status nvfp4_device_error(cudaStream_t stream, int *code);
 
 /* Self-test of the failure path (no fault involved): enqueues on `stream` one

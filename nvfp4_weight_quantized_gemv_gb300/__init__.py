@@ -15,6 +15,9 @@ import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libnvfp4_gemv.so")
+# the same library built with device index checks (buildlib.build(debug_bounds=True));
+# assign it to LIB_PATH before the first call to use it
+DEBUG_LIB_PATH = os.path.join(PKG, "libnvfp4_gemv_debug.so")
 
 # nvfp4_status
 NVFP4_OK = 0
@@ -25,6 +28,7 @@ NVFP4_ERR_CUDA = 4
 NVFP4_ERR_DEVICE_TIMEOUT = 5
 NVFP4_ERR_WORKSPACE = 6
 NVFP4_ERR_DEVICE_INPUT = 7
+NVFP4_ERR_DEVICE_BOUNDS = 8
 
 # nvfp4_variant / nvfp4_tiling
 VARIANT_AUTO, VARIANT_MMA, VARIANT_SIMT, VARIANT_GENERIC, VARIANT_TC, VARIANT_FP4 = 0, 1, 2, 3, 4, 5
@@ -307,11 +311,12 @@ def nvfp4_quantize_bf16(w, stream=None):
 
 def nvfp4_device_error(stream=None) -> int:
     """Synchronize, read and clear the device error word.  Returns the word
-    (0 = none; bits 8, 16 and 32 flag inputs a kernel could not use) and raises
-    Nvfp4Error when a kernel gave up on a wait (bits 1, 2, 4)."""
+    (0 = none; bits 8, 16 and 32 flag inputs a kernel could not use, bit 128 a
+    failed index check of the debug-bounds build) and raises Nvfp4Error when a
+    kernel gave up on a wait (bits 1, 2, 4)."""
     code = ctypes.c_int(0)
     st = lib().nvfp4_device_error(_stream_handle(stream), ctypes.byref(code))
-    if st not in (NVFP4_OK, NVFP4_ERR_DEVICE_TIMEOUT, NVFP4_ERR_DEVICE_INPUT):
+    if st not in (NVFP4_OK, NVFP4_ERR_DEVICE_TIMEOUT, NVFP4_ERR_DEVICE_INPUT, NVFP4_ERR_DEVICE_BOUNDS):
         _check(st)
     if st == NVFP4_ERR_DEVICE_TIMEOUT:
         raise Nvfp4Error(st, nvfp4_last_error())

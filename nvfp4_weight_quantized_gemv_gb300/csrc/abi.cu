@@ -937,6 +937,9 @@ extern "C" nvfp4_status nvfp4_device_error(cudaStream_t stream, int *code) {
     if (word == 0) return NVFP4_OK;
     const unsigned zero = 0;
     cudaMemcpy(d->err_word, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if ((word & 7u) == 0 && (word & 128u) != 0)  // a debug-bounds check failed
+        return fail(NVFP4_ERR_DEVICE_BOUNDS, "a device index check of the debug-bounds build failed and its access "
+                    "was skipped (error word 0x%x)", word);
     if ((word & 7u) == 0 && (word & 64u) != 0)
         return fail(NVFP4_ERR_UNSUPPORTED, "the GEMV found its dynamic shared memory off a 1024-byte boundary "
                     "and computed nothing (error word 0x%x)", word);

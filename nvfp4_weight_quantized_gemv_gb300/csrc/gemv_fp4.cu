@@ -237,10 +237,11 @@ __device__ __forceinline__ void f4_load_part(const F4Params &p, float (&part)[16
     const int crb0 = (int)(cu0 / KC);
     const float4 *src = reinterpret_cast<const float4 *>(p.partials + ((size_t)c * 2 + (rb == crb0 ? 0 : 1)) *
                                                                          (kUnitRows * 16) + (size_t)r * 16);
+    const bool in = nvfp4_in_bounds(c >= 0 && c < p.ctas && r >= 0 && r < kUnitRows, p.err);
 #pragma unroll
     for (int qd = 0; qd < 4; ++qd) {
         float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (4 * qd < p.n) f = __ldcg(src + qd);
+        if (in && 4 * qd < p.n) f = __ldcg(src + qd);
         part[4 * qd] = f.x;
         part[4 * qd + 1] = f.y;
         part[4 * qd + 2] = f.z;
@@ -262,7 +263,7 @@ __device__ __forceinline__ void f4_sum_parts(const F4Params &p, float (&sum)[16]
 #pragma unroll
         for (int j = 0; j < B; ++j) {
             const int c = c0 + j;
-            if (c <= cb && c != self) {
+            if (c <= cb && c != self && nvfp4_in_bounds(c >= 0 && c < p.ctas, p.err)) {
                 const long long cu0 = (long long)c * U / p.ctas;
                 const int crb0 = (int)(cu0 / KC);
                 const float4 *src = reinterpret_cast<const float4 *>(
@@ -957,6 +958,8 @@ __global__ void __maxnreg__(128)
             const int rb = ord.rb0 + ns;
             const int len = ord.seg_len(ns);
             const bool whole = len == KC;
+            // the row block's counter, partial tiles and rows (the same for the four warps)
+            if (!nvfp4_in_bounds(rb >= 0 && rb < p.row_blocks, p.err)) break;
             const long long ub = (long long)rb * KC;
             const int ca = (int)(((ub + 1) * p.ctas - 1) / U), cb = (int)(((ub + KC) * p.ctas - 1) / U);
             const int sb = s & 1;

@@ -260,6 +260,10 @@ __device__ __forceinline__ void flush_tile(const StreamParams &p, float (&v)[16]
         const int cfirst = cta_of_unit(ufirst, p.units, p.ctas);
         const int clast = cta_of_unit(ufirst + p.KC - 1, p.units, p.ctas);
         const int slot = ((int)blockIdx.x == cfirst) ? 1 : 0;
+        // the tile's counter and the parts' slots
+        if (!nvfp4_in_bounds(cfirst >= 0 && clast < p.ctas && cfirst <= (int)blockIdx.x &&
+                                 (int)blockIdx.x <= clast, p.err))
+            return;
         float4 *mine = reinterpret_cast<float4 *>(
             p.partials + (((size_t)blockIdx.x * 2 + slot) * kConsumerWarps + warp) * kSlotFloats + lane * 16);
 #pragma unroll

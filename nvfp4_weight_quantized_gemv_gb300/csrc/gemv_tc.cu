@@ -667,9 +667,11 @@ __global__ void __maxnreg__(kTcMaxRegs)
                     // one part of a split row block: publish the fp32 tile (T tokens per row);
                     // the reduction kernel that follows sums the parts in CTA order
                     float4 *const dst = reinterpret_cast<float4 *>(mine + 16 * c);
+                    const bool in = nvfp4_in_bounds(rb - rb0 >= 0 && rb - rb0 < part.max_seg, p.err);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        if (q < T / 4) __stcg(dst + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+                        if (in && q < T / 4)
+                            __stcg(dst + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
                 }
             }
             i = iend + 1;
@@ -742,10 +744,12 @@ __device__ __forceinline__ void tc_reduce_sweep(const StreamParams &p, const TcP
 #pragma unroll
         for (int j = 0; j < kChunk; ++j) {
             if (j0 + j < np) {
+                const int tile = cur.next(part);
                 const float4 *src = reinterpret_cast<const float4 *>(
-                    p.partials + (size_t)cur.next(part) * tc_partial_floats(T) + (size_t)r * T + h * TT);
+                    p.partials + (size_t)tile * tc_partial_floats(T) + (size_t)r * T + h * TT);
+                const bool in = nvfp4_in_bounds(tile >= 0 && tile < p.ctas * part.max_seg, p.err);
 #pragma unroll
-                for (int q = 0; q < kQ; ++q) f[j][q] = __ldcg(src + q);
+                for (int q = 0; q < kQ; ++q) f[j][q] = in ? __ldcg(src + q) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
 #pragma unroll

@@ -12,6 +12,22 @@ namespace nvfp4 {
 constexpr unsigned kDevErrTimeoutFull = 1u;    // consumer gave up waiting for a TMA stage
 constexpr unsigned kDevErrTimeoutEmpty = 2u;   // producer gave up waiting for a free stage
 constexpr unsigned kDevErrTimeoutDrain = 4u;   // copies still in flight at exit
+constexpr unsigned kDevErrBounds = 128u;       // debug builds: an index check skipped an access
+
+// Index checks of the kernels' computed workspace accesses (partial tiles,
+// split-row counters), compiled in by -DNVFP4_DEBUG_BOUNDS: a failed check
+// sets kDevErrBounds in the device error word and the caller skips the
+// access (never a trap).  Release builds: always true, compiled away.
+__device__ __forceinline__ bool nvfp4_in_bounds(bool ok, unsigned *err) {
+#ifdef NVFP4_DEBUG_BOUNDS
+    if (!ok) atomicOr(err, kDevErrBounds);
+    return ok;
+#else
+    (void)ok;
+    (void)err;
+    return true;
+#endif
+}
 
 // Wall-clock limit for any single wait, in nanoseconds (2 s).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;

@@ -44,6 +44,15 @@ def test_library_exports_every_declared_symbol():
     assert nv.nvfp4_version() >= 100
 
 
+def test_debug_bounds_build_exports_the_same_symbols():
+    from nvfp4_weight_quantized_gemv_gb300 import buildlib
+    path = buildlib.build(debug_bounds=True)
+    assert path == nv.DEBUG_LIB_PATH
+    L = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
 def test_validation_errors_without_gpu():
     L = nv.lib()
     p = ctypes.c_void_p(16)
