@@ -257,45 +257,71 @@ def _oracle_init(spec, cores):
     _ORACLE_TASKS = tasks
 
 
-def _oracle_run(i):
+def _oracle_run(task):
+    """Task (i, rows): the first `rows` rows of sampled chunk i."""
     import oracle
+    i, rows = task
     packed, scale, g, x = _ORACLE_TASKS[i]
-    oracle.gemv_rows(packed, scale, g, x)
+    oracle.gemv_rows(packed[:rows], scale[:rows], g, x)
     return i
 
 
-def cpu_oracle_sample(calls, rows_per_core: int, cores: int, repeats: int = 3):
+def cpu_oracle_sample(calls, rows_per_core: int, cores: int, repeats: int = 3, warmup: int = 1,
+                      step_budget_s=None):
     """Time the CPU oracle on a bounded sample of one step of the workload.
 
-    For every call of the step, `rows_per_core * cores` output rows (all of the
-    call's tokens) are computed by the fp64 oracle, split over `cores` spawned
-    processes that hold the sampled inputs already.  The sample is timed
-    `repeats` times after one untimed pass.  Returns (GB/s of the sampled
-    algorithmic bytes at the median wall time, median wall seconds, all wall
-    seconds, description)."""
+    For every call of the step, up to `rows_per_core * cores` output rows (all
+    of the call's tokens) are computed by the fp64 oracle, split over `cores`
+    spawned processes that hold the sampled inputs already.  `warmup` untimed
+    passes, then `repeats` timed ones.  With `step_budget_s`, the timed passes
+    compute only as many rows of each chunk as the last warm-up pass says fit
+    in that budget.  Returns (GB/s of the sampled algorithmic bytes at the
+    median wall time, median wall seconds, all wall seconds, description)."""
     import oracle
     oracle.build()
-    spec, nbytes = [], 0
+    spec = []
     for ci, (shape, n) in enumerate(calls):
         N, K = SHAPES[shape]
-        rows = min(N, rows_per_core * cores)
-        spec.append((N, K, n, OUTLIER[shape], rows, 1000 + ci))
-        nbytes += rows * (K // 2 + K // 16) + 2 * n * K
-    ntasks = sum(-(-s[4] // -(-s[4] // cores)) for s in spec)
+        spec.append((N, K, n, OUTLIER[shape], min(N, rows_per_core * cores), 1000 + ci))
+    chunks = []  # (call index, rows of the chunk)
+    for ci, (N, K, n, _, rows, _) in enumerate(spec):
+        per = -(-rows // cores)
+        chunks += [(ci, min(per, rows - r0)) for r0 in range(0, rows, per)]
+
+    def step_bytes(cap):
+        nb = 0
+        for ci, (N, K, n, _, _, _) in enumerate(spec):
+            r = sum(min(cap, c) for cj, c in chunks if cj == ci)
+            nb += r * (K // 2 + K // 16) + 2 * n * K
+        return nb
+
     ctx = mp.get_context("spawn")
     walls = []
+    full = max(c for _, c in chunks)
     with ctx.Pool(cores, initializer=_oracle_init, initargs=(spec, cores)) as pool:
-        pool.map(_oracle_run, range(ntasks), chunksize=1)  # untimed pass (also waits for every initializer)
+        cap = full
+        for w in range(max(1, warmup)):  # untimed; the first also waits for every initializer
+            t0 = time.perf_counter()
+            pool.map(_oracle_run, [(i, cap) for i in range(len(chunks))], chunksize=1)
+            t_warm = time.perf_counter() - t0
+            if w < 2 and step_budget_s is not None:  # the first two full passes size the sample
+                cap_next = max(1, min(full, int(full * step_budget_s / max(t_warm, 1e-6))))
+                cap = full if w == 0 else cap_next
+                if w == 0 and warmup == 1:
+                    cap = cap_next
+        tasks = [(i, cap) for i in range(len(chunks))]
         for _ in range(repeats):
             t0 = time.perf_counter()
-            pool.map(_oracle_run, range(ntasks), chunksize=1)
+            pool.map(_oracle_run, tasks, chunksize=1)
             walls.append(time.perf_counter() - t0)
     wall = statistics.median(walls)
+    rows_step = sum(min(cap, c) for _, c in chunks) // max(1, len(calls))
     names = ", ".join(f"{s} n={n}" for s, n in calls[:8]) + ("..." if len(calls) > 8 else "")
-    sample = (f"{rows_per_core * cores} output rows (all tokens) of each of the {len(calls)} calls of one step "
+    sample = (f"{rows_step} output rows (all tokens) of each of the {len(calls)} calls of one step "
               f"({names}); fp64 oracle over {cores} spawned processes holding the inputs; median of {repeats} "
-              f"timed repeats; GB/s of the sampled rows' weight+scale+activation bytes")
-    return nbytes / wall / 1e9, wall, walls, sample
+              f"timed repeats after {max(1, warmup)} untimed; GB/s of the sampled rows' weight+scale+activation "
+              f"bytes")
+    return step_bytes(cap) / wall / 1e9, wall, walls, sample
 
 
 # --------------------------------------------------- oracle check of outputs
@@ -697,18 +723,22 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        # each timed repeat is a bounded sample (cpu_rows rows per core of every
-        # call); at least 3 and at most 5 repeats, so the run ends within minutes
-        repeats = max(3, min(args.steps, 5))
-        gbs, wall, walls, sample = cpu_oracle_sample(cpu_calls, args.cpu_rows, cores, repeats=repeats)
+        # exactly --warmup untimed and --steps timed steps, each a bounded
+        # sample of the step (rows per chunk sized from the last warm-up step
+        # so that the timed steps take about half a minute in all)
+        budget = min(0.3, max(0.002, 30.0 / max(1, args.steps)))
+        gbs, wall, walls, sample = cpu_oracle_sample(cpu_calls, args.cpu_rows, cores, repeats=args.steps,
+                                                     warmup=args.warmup, step_budget_s=budget)
         line = {"metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
-                "steps": repeats, "warmup": 1, "ms_per_step": round(wall * 1e3, 3),
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall * 1e3, 3),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic (seeded PCG64: W~N(0,0.02) quantized to NVFP4, X~N(0,1) bf16)",
                 "config": {"workload": wl_desc, "tiling": "per token (each output computed on its own)",
                            "sample_per_step": sample},
                 "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                 "sample": sample, "repeat_walls_s": [round(w, 3) for w in walls]},
+                                 "sample": sample,
+                                 "step_walls_s": {"min": round(min(walls), 4), "median": round(wall, 4),
+                                                  "max": round(max(walls), 4)}},
                 "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                 "gpu_launches": 0}
         print(json.dumps(line), flush=True)
