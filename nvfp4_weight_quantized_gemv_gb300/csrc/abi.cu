@@ -490,8 +490,8 @@ static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nv
         // small X term blocks stay resident for the whole call (a few bulk
         // copies per CTA instead of one per unit)
         p.f4_x_resident = (long long)KC * f4_slot_bytes(p.f4_cols_max) <= kF4ResidentXMax &&
-                          f4_max_stages(p.f4_cols_max, limit, true, KC) >= 4;
-        const int max_stages = f4_max_stages(p.f4_cols_max, limit, p.f4_x_resident, KC);
+                          f4_max_stages(p.f4_cols_max, limit, true, KC, p.f4_cluster) >= 4;
+        const int max_stages = f4_max_stages(p.f4_cols_max, limit, p.f4_x_resident, KC, p.f4_cluster);
         if (max_stages < 2) return fail(NVFP4_ERR_UNSUPPORTED, "the FP4 kernel does not fit shared memory");
         int stages = max_stages;
         if (o.stages != 0) {
@@ -501,7 +501,7 @@ static nvfp4_status make_plan_tokens(int n, int N, int K, bool fast_ok, const nv
         }
         p.stages = stages;
         p.f4_inflight = o.inflight > 0 ? o.inflight : kF4DefaultInflight;
-        p.smem = f4_smem_bytes(stages, p.f4_cols_max, p.f4_x_resident, KC);
+        p.smem = f4_smem_bytes(stages, p.f4_cols_max, p.f4_x_resident, KC, p.f4_cluster);
         const int RB = (N + kUnitRows - 1) / kUnitRows;
         p.counter_bytes = ws_counter_bytes(sms, RB);
         p.partial_bytes = (size_t)ctas * 2 * kUnitRows * 16 * sizeof(float);  // first and last row block
@@ -671,7 +671,8 @@ static nvfp4_status run(const uint8_t *wp, const uint8_t *ws, const float *gs, c
             fp.cols = f4_cols(tn);
             fp.w_keep = (t0 + tn < n) ? 1 : 0;  // the next pass re-reads W: from L2, not HBM
             if ((e = launch_fp4(tw, ts, x + (size_t)t0 * K, fp,
-                                f4_smem_bytes(plan.stages, fp.cols, plan.f4_x_resident, fp.KC), stream)) !=
+                                f4_smem_bytes(plan.stages, fp.cols, plan.f4_x_resident, fp.KC, plan.f4_cluster),
+                                stream)) !=
                 cudaSuccess)
                 return cuda_fail(e, "FP4 kernel launch");
             t0 += tn;

@@ -298,52 +298,38 @@ __device__ __forceinline__ void f4_sum_parts(const F4Params &p, float (&sum)[16]
     for (int t = 4 * KQ; t < 16; ++t) sum[t] = 0.f;
 }
 
-// Sum of the `cl` parts of this thread's row held by the CTAs of its cluster
-// (shared-memory address `mine` in each), in rank order: the same order,
-// and so the same rounding, as the workspace path's CTA order.  The loads of
-// up to 8 / KQ parts are in flight together.
+// The cluster's sum of this thread's row over its `cl` parts, in rank order
+// (the same order, and so the same rounding, as the workspace path's CTA
+// order), stored: part `rank` (this CTA's own) at `own` in ring stage 0, the
+// peers' parts in this CTA's receive area at `recv` + slot * `slot_stride`
+// (slot = sender rank, less one above this CTA's rank).  Local shared-memory
+// loads only: the peers pushed their parts before the cluster barrier.
 template <int KQ>
-__device__ __forceinline__ void f4_sum_cluster(float (&sum)[16], uint32_t mine, int cl) {
-    constexpr int B = 8 / KQ;
-    for (int k0 = 0; k0 < cl; k0 += B) {
-        float4 f[B][KQ];
+__device__ __forceinline__ void f4_cluster_finish(const F4Out p, uint32_t own, uint32_t recv, uint32_t slot_stride,
+                                                  int rank, int cl, int row, float g) {
+    float sum[16];
+    for (int k = 0; k < cl; ++k) {
+        const uint32_t src = k == rank ? own : recv + (uint32_t)(k < rank ? k : k - 1) * slot_stride;
 #pragma unroll
-        for (int j = 0; j < B; ++j) {
-            if (k0 + j < cl) {
-                const uint32_t src = cluster_map(mine, (uint32_t)(k0 + j));
-#pragma unroll
-                for (int qd = 0; qd < KQ; ++qd) f[j][qd] = ld_cluster_f4(src + 16 * qd);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < B; ++j) {
-            if (k0 + j >= cl) break;
-#pragma unroll
-            for (int qd = 0; qd < KQ; ++qd) {
-                const float4 v = f[j][qd];
-                if (k0 + j == 0) {
-                    sum[4 * qd] = v.x;
-                    sum[4 * qd + 1] = v.y;
-                    sum[4 * qd + 2] = v.z;
-                    sum[4 * qd + 3] = v.w;
-                } else {
-                    sum[4 * qd] += v.x;
-                    sum[4 * qd + 1] += v.y;
-                    sum[4 * qd + 2] += v.z;
-                    sum[4 * qd + 3] += v.w;
-                }
+        for (int qd = 0; qd < KQ; ++qd) {
+            const uint4 u = lds128(src + 16 * qd);
+            const float4 v = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                                         __uint_as_float(u.w));
+            if (k == 0) {
+                sum[4 * qd] = v.x;
+                sum[4 * qd + 1] = v.y;
+                sum[4 * qd + 2] = v.z;
+                sum[4 * qd + 3] = v.w;
+            } else {
+                sum[4 * qd] += v.x;
+                sum[4 * qd + 1] += v.y;
+                sum[4 * qd + 2] += v.z;
+                sum[4 * qd + 3] += v.w;
             }
         }
     }
 #pragma unroll
     for (int t = 4 * KQ; t < 16; ++t) sum[t] = 0.f;
-}
-
-// The cluster's sum of this thread's row, stored.
-template <int KQ>
-__device__ __forceinline__ void f4_cluster_finish(const F4Out p, uint32_t mine, int cl, int row, float g) {
-    float sum[16];
-    f4_sum_cluster<KQ>(sum, mine, cl);
     f4_store_row(p, sum, row, g);
 }
 
@@ -370,22 +356,23 @@ __device__ __forceinline__ uint32_t f4_cvt_e2m1x8(const float (&q)[8]) {
 // they are streamed), the resident X codes (all K / 256 unit columns) when not,
 // the X block scales of all unit columns, the barriers, then flags and the
 // term scales.
-int f4_smem_bytes(int stages, int cols, bool x_resident, int KC) {
+int f4_smem_bytes(int stages, int cols, bool x_resident, int KC, int cluster) {
     const int slot = f4_slot_bytes(cols), groups = (KC + kF4XGroup - 1) / kF4XGroup;
     const int xbars = x_resident ? (groups > stages ? groups : stages) : stages;
     const int tabs = (KC * f4_tab_bytes(cols) + 15) & ~15;
     return stages * (kF4XOffHost + (x_resident ? 0 : slot)) + (x_resident ? KC * slot : 0) + tabs +
-           8 * (3 * stages + xbars + 9) + kF4MiscBytes;
+           8 * (3 * stages + xbars + 9) + kF4MiscBytes + f4_red_bytes(cluster);
 }
 
 // TMEM: accumulators [issuer][segment buffer 2][f4_dstride(cols)] from column
 // 0, then kF4SfCols per stage (W scales, then X block scales).
-int f4_max_stages(int cols, int smem_limit, bool x_resident, int KC) {
+int f4_max_stages(int cols, int smem_limit, bool x_resident, int KC, int cluster) {
     const int tmem_stages = ((int)kF4TmemCols - 2 * f4_issuers(cols) * f4_dstride(cols)) / kF4SfCols;
     int s = 2;
-    while (s + 1 <= tmem_stages && s + 1 <= kF4MaxStages && f4_smem_bytes(s + 1, cols, x_resident, KC) <= smem_limit)
+    while (s + 1 <= tmem_stages && s + 1 <= kF4MaxStages &&
+           f4_smem_bytes(s + 1, cols, x_resident, KC, cluster) <= smem_limit)
         ++s;
-    return f4_smem_bytes(s, cols, x_resident, KC) <= smem_limit ? s : 0;
+    return f4_smem_bytes(s, cols, x_resident, KC, cluster) <= smem_limit ? s : 0;
 }
 
 // ------------------------------------------------------------------ X prep
@@ -613,10 +600,8 @@ __global__ void __maxnreg__(128)
     if (sbase & 1023u) {  // the swizzled tiles need a 1024-byte aligned base; never expected
         griddep_wait();
         if (threadIdx.x == 0) atomicOr(p.err, kF4ErrSmemBase);
-        if (p.cluster) {  // every CTA of the cluster takes this path (same layout): both cluster phases
+        if (p.cluster) {  // every CTA of the cluster takes this path (same layout): the cluster phase
             __syncwarp();
-            cluster_arrive();
-            cluster_wait();
             cluster_arrive();
             cluster_wait();
         }
@@ -707,15 +692,18 @@ __global__ void __maxnreg__(128)
     const uint32_t sf_base = tbase + 2 * kIssuers * kDStride;
 
     // Split row blocks summed in a cluster (p.cluster = p CTAs per row block,
-    // one segment each): the epilogue leaves this CTA's part in ring stage 0
-    // (free once the segment's MMAs are done); after a cluster barrier the
-    // CTA of rank k sums the rows of its epilogue warps q with q % p == k
-    // over the p parts in rank (= CTA) order and stores them; a second
-    // barrier keeps every CTA alive until its peers have read its part.
-    // (Measured on GB300: the hardware cluster barrier beat remote mbarrier
-    // arrivals here by ~1.2 us per call.)
+    // one segment each): the rows of epilogue warp q are summed by the CTA of
+    // rank q % p.  Each CTA's epilogue leaves its part of its own rows in
+    // ring stage 0 (free once the segment's MMAs are done) and pushes its part
+    // of the other rows into their CTA's receive area (distributed shared
+    // memory stores); after one cluster barrier every CTA sums its rows over
+    // the p parts in rank (= CTA) order from its own shared memory and stores
+    // them.  (Measured on GB300: the hardware cluster barrier beat remote
+    // mbarrier arrivals here by ~1.2 us per call.)
     const int cl = p.cluster;
     const uint32_t sRed = sbase;  // [128 rows][16] fp32, a row's tokens in 64 bytes
+    const uint32_t sRecv = (sMisc + kF4MiscBytes + 15u) & ~15u;  // the peers' parts ([cl - 1][red_rows][16] fp32)
+    const int red_rows = cl ? 32 * ((4 + cl - 1) / cl) : 0;
     bool red_pending = false;
     int red_row = 0;
     float g_ep = 0.f;
@@ -1060,12 +1048,27 @@ __global__ void __maxnreg__(128)
                 continue;
             }
             if (cl) {  // the cluster sums the parts after the loop
+                // the rows of warp q are summed by the CTA of rank q % cl: its
+                // own part stays in its ring stage 0, the others are pushed
+                // into its receive area (slot = sender rank, less one above it)
+                const int rank = (int)cluster_ctarank(), k = q % cl;
+                if (k == rank) {
 #pragma unroll
-                for (int qd = 0; qd < 4; ++qd)
-                    if (4 * qd < p.n)
-                        sts128(sRed + (uint32_t)r * 64 + 16 * qd,
-                               make_uint4(__float_as_uint(acc[4 * qd]), __float_as_uint(acc[4 * qd + 1]),
-                                          __float_as_uint(acc[4 * qd + 2]), __float_as_uint(acc[4 * qd + 3])));
+                    for (int qd = 0; qd < 4; ++qd)
+                        if (4 * qd < p.n)
+                            sts128(sRed + (uint32_t)r * 64 + 16 * qd,
+                                   make_uint4(__float_as_uint(acc[4 * qd]), __float_as_uint(acc[4 * qd + 1]),
+                                              __float_as_uint(acc[4 * qd + 2]), __float_as_uint(acc[4 * qd + 3])));
+                } else {
+                    const uint32_t slot = (uint32_t)(rank < k ? rank : rank - 1);
+                    const uint32_t dst = cluster_map(
+                        sRecv + (slot * (uint32_t)red_rows + (uint32_t)((q / cl) * 32 + lane)) * 64, (uint32_t)k);
+#pragma unroll
+                    for (int qd = 0; qd < 4; ++qd)
+                        if (4 * qd < p.n)
+                            st_cluster_f4(dst + 16 * qd, acc[4 * qd], acc[4 * qd + 1], acc[4 * qd + 2],
+                                          acc[4 * qd + 3]);
+                }
                 red_pending = true;
                 red_row = row;
                 continue;
@@ -1113,27 +1116,24 @@ __global__ void __maxnreg__(128)
     }
 
     if (cl) {
-        // every part of the cluster's row blocks is in its CTA's shared memory
+        // every CTA's parts are in the shared memory of the CTAs that sum them
         // (the hardware cluster barrier: every thread of the cluster arrives,
-        // and every CTA gets here, since all its own waits are bounded)
+        // and every CTA gets here, since all its own waits are bounded; after
+        // it no CTA touches another's shared memory, so none waits to leave)
         __syncwarp();
         cluster_arrive();
         cluster_wait();
-        const int q = warp & 3;
-        if (warp >= kF4WarpEpi0 && warp < kF4WarpEpi0 + 4 && q % cl == (int)cluster_ctarank() && red_pending)
-            f4_cluster_finish<(NC / kF4Terms + 3) / 4>(F4Out{p.y, p.N, p.n, p.swiglu},
-                                                       sRed + (uint32_t)(32 * q + lane) * 64, cl, red_row, g_ep);
+        const int q = warp & 3, rank = (int)cluster_ctarank();
+        if (warp >= kF4WarpEpi0 && warp < kF4WarpEpi0 + 4 && q % cl == rank && red_pending)
+            f4_cluster_finish<(NC / kF4Terms + 3) / 4>(
+                F4Out{p.y, p.N, p.n, p.swiglu}, sRed + (uint32_t)(32 * q + lane) * 64,
+                sRecv + (uint32_t)((q / cl) * 32 + lane) * 64, (uint32_t)red_rows * 64, rank, cl, red_row, g_ep);
     }
     tc::fence_before_sync();
     __syncthreads();
     if (warp == kF4WarpIssuer) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tbase, kF4TmemCols);
-    }
-    if (cl) {  // no CTA leaves while a peer may still read its part
-        __syncwarp();
-        cluster_arrive();
-        cluster_wait();
     }
 }
 

@@ -88,8 +88,14 @@ struct F4Params {
     int cluster;          // p >= 2: every row block is split over p consecutive CTAs, launched as one
                           // cluster that sums the parts through distributed shared memory; 0: no clusters
 };
-int f4_smem_bytes(int stages, int cols, bool x_resident, int KC);
-int f4_max_stages(int cols, int smem_limit, bool x_resident, int KC);   // 0: does not fit
+// Cluster sums of split row blocks (p CTAs per row block): the CTA of rank k
+// sums the rows of epilogue warps q with q % p == k; its peers push their
+// parts of those rows into its receive area, [p - 1 senders][f4_red_rows(p)
+// rows][16 fp32], after the misc area (16-byte aligned).
+inline int f4_red_rows(int p) { return p >= 2 ? 32 * ((4 + p - 1) / p) : 0; }
+inline int f4_red_bytes(int p) { return p >= 2 ? (p - 1) * f4_red_rows(p) * 64 + 16 : 0; }
+int f4_smem_bytes(int stages, int cols, bool x_resident, int KC, int cluster = 0);
+int f4_max_stages(int cols, int smem_limit, bool x_resident, int KC, int cluster = 0);  // 0: does not fit
 cudaError_t f4_set_smem_limit(int smem_optin);
 // X prep then GEMV, both with programmatic dependent launch.
 cudaError_t launch_fp4(const CUtensorMap &tw, const CUtensorMap &ts, const uint16_t *x, const F4Params &p, int smem,
